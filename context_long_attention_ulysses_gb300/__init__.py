@@ -1,0 +1,219 @@
+"""Ulysses sequence-parallel attention on one GB300 -- Python binding of libusp.
+
+The functions named ``usp_*`` mirror the C ABI in ``include/usp.h`` one to
+one: they only marshal arguments (torch tensors or raw device pointers, the
+current torch stream) and raise :class:`UspError` on a non-OK status.  Every
+step of the computation runs in libusp's CUDA kernels; PyTorch provides
+device memory and streams.
+
+The helpers ``ulysses_attention_fwd``/``ulysses_attention_bwd`` and
+``ring_attention_fwd`` chain those calls the way one sequence-parallel
+attention layer does (all-to-all, attention, all-to-all back) and allocate
+their outputs with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import torch
+
+from ._lib import (SYMBOLS, USP_BF16, USP_F32, USP_OK, UspError, UspProblem, check, load)  # noqa: F401
+
+__all__ = [
+    "Problem", "UspError", "SYMBOLS",
+    "usp_a2a_seq2head", "usp_a2a_head2seq", "usp_attn_fwd", "usp_attn_bwd_workspace_size", "usp_attn_bwd",
+    "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
+    "usp_build_info", "ulysses_attention_fwd", "ulysses_attention_bwd", "ring_attention_fwd", "library_path",
+]
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class Problem:
+    """Q: B x Hq x N x d, K/V: B x Hkv x N x d, sequence-parallel degree P."""
+    B: int
+    Hq: int
+    Hkv: int
+    N: int
+    d: int
+    P: int
+    causal: bool = True
+    scale: float = 0.0  # 0 selects 1/sqrt(d)
+    dtype: str = "bf16"
+
+    def c(self) -> UspProblem:
+        if self.dtype not in _TORCH_DTYPE:
+            raise ValueError(f"dtype must be 'f32' or 'bf16', got {self.dtype!r}")
+        return UspProblem(self.B, self.Hq, self.Hkv, self.N, self.d, self.P, int(bool(self.causal)),
+                          float(self.scale), USP_F32 if self.dtype == "f32" else USP_BF16)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPE[self.dtype]
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale else 1.0 / math.sqrt(self.d)
+
+    def seq_shape(self, H: int):
+        """Sequence-sharded layout [P][B][N/P][H][d]."""
+        return (self.P, self.B, self.N // self.P, H, self.d)
+
+    def head_shape(self, H: int):
+        """Head-sharded layout [P][B][H/P][N][d]."""
+        return (self.P, self.B, H // self.P, self.N, self.d)
+
+    def lse_head_shape(self):
+        return (self.P, self.B, self.Hq // self.P, self.N)
+
+    def lse_seq_shape(self):
+        return (self.P, self.B, self.N // self.P, self.Hq)
+
+
+def library_path() -> str:
+    from .build import LIB
+    return LIB
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if isinstance(x, torch.Tensor):
+        if x.numel() and not x.is_cuda:
+            raise ValueError("libusp takes device tensors")
+        if not x.is_contiguous():
+            raise ValueError("libusp takes contiguous tensors")
+        return x.data_ptr()
+    raise TypeError(f"expected a torch tensor, a device pointer or None, got {type(x).__name__}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _prob(p) -> ctypes.POINTER(UspProblem):
+    if p is None:
+        return None
+    return ctypes.byref(p.c() if isinstance(p, Problem) else p)
+
+
+# --------------------------------------------------------------- C ABI mirror
+def usp_a2a_seq2head(p, Hx: int, src, dst, stream=None) -> None:
+    check("usp_a2a_seq2head", load().usp_a2a_seq2head(_prob(p), Hx, _ptr(src), _ptr(dst), _stream(stream)))
+
+
+def usp_a2a_head2seq(p, Hx: int, src, dst, stream=None) -> None:
+    check("usp_a2a_head2seq", load().usp_a2a_head2seq(_prob(p), Hx, _ptr(src), _ptr(dst), _stream(stream)))
+
+
+def usp_attn_fwd(p, q, k, v, o, lse, stream=None) -> None:
+    check("usp_attn_fwd", load().usp_attn_fwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                              _stream(stream)))
+
+
+def usp_attn_bwd_workspace_size(p) -> int:
+    return int(load().usp_attn_bwd_workspace_size(_prob(p)))
+
+
+def usp_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_attn_bwd", load().usp_attn_bwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
+                                              _stream(stream)))
+
+
+def usp_ring_workspace_size(p) -> int:
+    return int(load().usp_ring_workspace_size(_prob(p)))
+
+
+def usp_ring_attn_fwd(p, q, k, v, o, lse, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_ring_attn_fwd", load().usp_ring_attn_fwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                        _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def usp_ring_merge(rows: int, d: int, o_a, lse_a, o_b, lse_b, o, lse, stream=None) -> None:
+    check("usp_ring_merge", load().usp_ring_merge(int(rows), int(d), _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b),
+                                                  _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def usp_device_status(stream=None) -> int:
+    return int(load().usp_device_status(_stream(stream)))
+
+
+def usp_status_string(s: int) -> str:
+    return load().usp_status_string(int(s)).decode()
+
+
+def usp_build_info() -> str:
+    return load().usp_build_info().decode()
+
+
+# ------------------------------------------------------------ layer helpers
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def ulysses_attention_fwd(p: Problem, q_seq, k_seq, v_seq, stream=None):
+    """One Ulysses attention forward on sequence-sharded Q, K, V.
+
+    seq->head all-to-all of Q, K, V; attention per rank; head->seq all-to-all
+    of O.  Returns (o_seq, saved) where ``saved`` holds the head-sharded
+    tensors and LSE the backward needs.
+    """
+    dev, dt = q_seq.device, p.torch_dtype
+    qh = _empty(p.head_shape(p.Hq), dt, dev)
+    kh = _empty(p.head_shape(p.Hkv), dt, dev)
+    vh = _empty(p.head_shape(p.Hkv), dt, dev)
+    oh = _empty(p.head_shape(p.Hq), dt, dev)
+    lse = _empty(p.lse_head_shape(), torch.float32, dev)
+    o_seq = _empty(p.seq_shape(p.Hq), dt, dev)
+    usp_a2a_seq2head(p, p.Hq, q_seq, qh, stream)
+    usp_a2a_seq2head(p, p.Hkv, k_seq, kh, stream)
+    usp_a2a_seq2head(p, p.Hkv, v_seq, vh, stream)
+    usp_attn_fwd(p, qh, kh, vh, oh, lse, stream)
+    usp_a2a_head2seq(p, p.Hq, oh, o_seq, stream)
+    return o_seq, {"q": qh, "k": kh, "v": vh, "o": oh, "lse": lse}
+
+
+def ulysses_attention_bwd(p: Problem, saved, do_seq, stream=None):
+    """Backward of :func:`ulysses_attention_fwd` for upstream gradient dO (sequence-sharded).
+
+    Returns (dq_seq, dk_seq, dv_seq).
+    """
+    dev, dt = do_seq.device, p.torch_dtype
+    doh = _empty(p.head_shape(p.Hq), dt, dev)
+    dqh = _empty(p.head_shape(p.Hq), dt, dev)
+    dkh = _empty(p.head_shape(p.Hkv), dt, dev)
+    dvh = _empty(p.head_shape(p.Hkv), dt, dev)
+    ws = torch.empty(max(usp_attn_bwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    usp_a2a_seq2head(p, p.Hq, do_seq, doh, stream)
+    usp_attn_bwd(p, saved["q"], saved["k"], saved["v"], saved["o"], saved["lse"], doh, dqh, dkh, dvh, ws, None, stream)
+    dq = _empty(p.seq_shape(p.Hq), dt, dev)
+    dk = _empty(p.seq_shape(p.Hkv), dt, dev)
+    dv = _empty(p.seq_shape(p.Hkv), dt, dev)
+    usp_a2a_head2seq(p, p.Hq, dqh, dq, stream)
+    usp_a2a_head2seq(p, p.Hkv, dkh, dk, stream)
+    usp_a2a_head2seq(p, p.Hkv, dvh, dv, stream)
+    return dq, dk, dv
+
+
+def ring_attention_fwd(p: Problem, q_seq, k_seq, v_seq, stream=None):
+    """Ring attention forward on sequence-sharded buffers: returns (o_seq, lse_seq)."""
+    dev, dt = q_seq.device, p.torch_dtype
+    o = _empty(p.seq_shape(p.Hq), dt, dev)
+    lse = _empty(p.lse_seq_shape(), torch.float32, dev)
+    ws = torch.empty(max(usp_ring_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    usp_ring_attn_fwd(p, q_seq, k_seq, v_seq, o, lse, ws, None, stream)
+    return o, lse

@@ -1,0 +1,326 @@
+// C-ABI layer of libusp: host-side validation, tensor-map encoding and
+// dispatch to the kernels.  Nothing is enqueued unless every argument checks
+// out; the library never allocates device memory.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/usp.h"
+#include "kernels.h"
+
+namespace usp {
+
+// Device status word (see ptx.cuh); one per device context.
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Address of the status word on the current device (looked up once per device).
+int* status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int dtype) { return dtype == USP_F32 ? 4 : (dtype == USP_BF16 ? 2 : 0); }
+
+// Sizes and divisibility shared by every problem-based entry point.
+usp_status check_problem(const usp_problem* p) {
+    if (!p) return USP_ERR_INVALID_ARG;
+    if (p->B < 0 || p->N < 0 || p->Hq < 1 || p->Hkv < 1 || p->P < 1) return USP_ERR_INVALID_ARG;
+    if (p->N % p->P != 0 || p->Hq % p->Hkv != 0 || p->Hq % p->P != 0 || p->Hkv % p->P != 0)
+        return USP_ERR_INVALID_ARG;
+    if (p->dtype != USP_F32 && p->dtype != USP_BF16) return USP_ERR_INVALID_ARG;
+    if (p->d < 1) return USP_ERR_INVALID_ARG;
+    if (!(p->scale >= 0.f) || std::isinf(p->scale)) return USP_ERR_INVALID_ARG;
+    if ((int64_t)p->B * p->Hq > 65535) return USP_ERR_UNSUPPORTED;  // grid.y limit
+    return USP_OK;
+}
+
+float eff_scale(const usp_problem* p) { return p->scale == 0.f ? 1.0f / std::sqrt((float)p->d) : p->scale; }
+
+bool empty(const usp_problem* p) { return p->B == 0 || p->N == 0; }
+
+usp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? USP_OK : USP_ERR_CUDA; }
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const Tensor4& t, int d, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)t.n_head, (cuuint64_t)t.n_tok, (cuuint64_t)t.n_outer};
+    cuuint64_t strides[3] = {(cuuint64_t)t.s_head * 2, (cuuint64_t)t.s_tok * 2, (cuuint64_t)t.s_outer * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.ptr, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace usp
+
+using namespace usp;
+
+extern "C" {
+
+const char* usp_status_string(usp_status s) {
+    switch (s) {
+        case USP_OK: return "USP_OK";
+        case USP_ERR_INVALID_ARG: return "USP_ERR_INVALID_ARG";
+        case USP_ERR_UNSUPPORTED: return "USP_ERR_UNSUPPORTED";
+        case USP_ERR_MISALIGNED: return "USP_ERR_MISALIGNED";
+        case USP_ERR_WORKSPACE: return "USP_ERR_WORKSPACE";
+        case USP_ERR_CUDA: return "USP_ERR_CUDA";
+        case USP_ERR_TIMEOUT: return "USP_ERR_TIMEOUT";
+    }
+    return "USP_ERR_UNKNOWN";
+}
+
+const char* usp_build_info(void) { return "libusp 0.1 sm_103a (tcgen05/TMEM/TMA attention, on-device all-to-all)"; }
+
+usp_status usp_device_status(usp_stream stream) {
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return USP_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, sp, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return USP_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(sp, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return USP_ERR_CUDA;
+        return USP_ERR_TIMEOUT;
+    }
+    return USP_OK;
+}
+
+static usp_status a2a(int dir, const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
+    usp_status st = check_problem(p);
+    if (st != USP_OK) return st;
+    if (Hx != p->Hq && Hx != p->Hkv) return USP_ERR_INVALID_ARG;
+    const int row_bytes = p->d * elem_size(p->dtype);
+    if (row_bytes != 64 && row_bytes != 128 && row_bytes != 256 && row_bytes != 512) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    if (!aligned16(src) || !aligned16(dst)) return USP_ERR_MISALIGNED;
+    const size_t bytes = (size_t)p->B * Hx * (size_t)p->N * row_bytes;
+    const char* s = static_cast<const char*>(src);
+    const char* t = static_cast<const char*>(dst);
+    if (s < t + bytes && t < s + bytes) return USP_ERR_INVALID_ARG;  // overlap
+    return cuda_status(launch_remap(dir, src, dst, p->B, Hx, p->N, p->P, row_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+usp_status usp_a2a_seq2head(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
+    return a2a(0, p, Hx, src, dst, stream);
+}
+
+usp_status usp_a2a_head2seq(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
+    return a2a(1, p, Hx, src, dst, stream);
+}
+
+// Head-sharded forward parameters: every (rank, batch, local head) is one
+// "head slot"; slots are contiguous [N][d] blocks.
+static FwdParams head_sharded_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int* status) {
+    FwdParams f{};
+    const int Zq = p->B * p->Hq;  // = P * B * Hq/P
+    const int Zk = p->B * p->Hkv;
+    const int64_t nd = (int64_t)p->N * p->d;
+    f.q = Tensor4{const_cast<void*>(q), nd, p->d, nd * Zq, Zq, p->N, 1};
+    f.k = Tensor4{const_cast<void*>(k), nd, p->d, nd * Zk, Zk, p->N, 1};
+    f.v = Tensor4{const_cast<void*>(v), nd, p->d, nd * Zk, Zk, p->N, 1};
+    f.d = p->d;
+    f.g = p->Hq / p->Hkv;
+    f.n_heads = Zq;
+    f.n_outer = 1;
+    f.q_len = p->N;
+    f.kv_len = p->N;
+    f.ring_i0 = 0;
+    f.ring_t = 0;
+    f.ring_p = 1;
+    f.bsz = 1;
+    f.np = 0;
+    f.causal = p->causal ? 1 : 0;
+    f.scale = eff_scale(p);
+    f.o_bf16 = o;
+    f.o_f32 = nullptr;
+    f.o_s_head = nd;
+    f.o_s_tok = p->d;
+    f.o_s_outer = nd * Zq;
+    f.lse = lse;
+    f.l_s_head = p->N;
+    f.l_s_tok = 1;
+    f.l_s_outer = (int64_t)p->N * Zq;
+    f.status = status;
+    return f;
+}
+
+usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                        usp_stream stream) {
+    usp_status st = check_problem(p);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return USP_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Zq = p->B * p->Hq;
+    if (p->dtype == USP_F32)
+        return cuda_status(launch_attn_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                               static_cast<const float*>(v), static_cast<float*>(o), lse, Zq,
+                                               p->Hq / p->Hkv, p->N, p->d, p->causal ? 1 : 0, eff_scale(p), s));
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    FwdParams f = head_sharded_fwd(p, q, k, v, o, lse, sp);
+    return cuda_status(launch_attn_fwd_bf16(f, s));
+}
+
+size_t usp_attn_bwd_workspace_size(const usp_problem* p) {
+    if (check_problem(p) != USP_OK) return 0;
+    // D_i and lse_i*log2(e) per query row, rows padded to whole 128-row tiles
+    const size_t npad = ((size_t)p->N + 127) / 128 * 128;
+    return ((2 * (size_t)p->B * p->Hq * npad * sizeof(float)) + 255) & ~(size_t)255;
+}
+
+usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        usp_stream stream) {
+    usp_status st = check_problem(p);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    if (ws_bytes < usp_attn_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    BwdParams b{};
+    b.q = q; b.k = k; b.v = v; b.o = o; b.dout = dout; b.lse = lse;
+    b.dvec = static_cast<float*>(ws);
+    b.dq = dq; b.dk = dk; b.dv = dv;
+    b.Zq = p->B * p->Hq;
+    b.g = p->Hq / p->Hkv;
+    b.N = p->N;
+    b.d = p->d;
+    b.causal = p->causal ? 1 : 0;
+    b.scale = eff_scale(p);
+    b.status = sp;
+    return cuda_status(launch_attn_bwd_bf16(b, static_cast<cudaStream_t>(stream)));
+}
+
+usp_status usp_ring_merge(int64_t rows, int d, const float* o_a, const float* lse_a, const float* o_b,
+                          const float* lse_b, float* o, float* lse, usp_stream stream) {
+    if (rows < 0 || d < 1 || d % 4 != 0) return USP_ERR_INVALID_ARG;
+    if (rows == 0) return USP_OK;
+    const void* ptrs[] = {o_a, lse_a, o_b, lse_b, o, lse};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    return cuda_status(launch_lse_merge(rows, d, o_a, lse_a, o_b, lse_b, o, lse, static_cast<cudaStream_t>(stream)));
+}
+
+// Ring workspace: float32 running output [rows][d], float32 partial output
+// [rows][d] and partial LSE [rows], rows = P*B*(N/P)*Hq in sequence-sharded
+// order.  The caller's lse buffer holds the running LSE.
+static size_t ring_part(size_t bytes) { return (bytes + 255) & ~(size_t)255; }
+
+size_t usp_ring_workspace_size(const usp_problem* p) {
+    if (check_problem(p) != USP_OK) return 0;
+    const size_t rows = (size_t)p->B * p->N * p->Hq;
+    return 2 * ring_part(rows * p->d * sizeof(float)) + ring_part(rows * sizeof(float));
+}
+
+usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                             void* ws, size_t ws_bytes, usp_stream stream) {
+    usp_status st = check_problem(p);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
+    if ((int64_t)p->B * p->P > 65535) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return USP_ERR_MISALIGNED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    if (ws_bytes < usp_ring_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d;
+    const int Np = p->N / P;
+    const size_t rows = (size_t)B * p->N * Hq;
+    float* acc_o = static_cast<float*>(ws);
+    float* part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + ring_part(rows * d * sizeof(float)));
+    float* part_l = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ring_part(rows * d * sizeof(float)));
+    const size_t rows_per_rank = (size_t)B * Np * Hq;
+
+    FwdParams f{};
+    f.q = Tensor4{const_cast<void*>(q), d, (int64_t)Hq * d, (int64_t)Np * Hq * d, Hq, Np, P * B};
+    f.k = Tensor4{const_cast<void*>(k), d, (int64_t)Hkv * d, (int64_t)Np * Hkv * d, Hkv, Np, P * B};
+    f.v = Tensor4{const_cast<void*>(v), d, (int64_t)Hkv * d, (int64_t)Np * Hkv * d, Hkv, Np, P * B};
+    f.d = d;
+    f.g = Hq / Hkv;
+    f.n_heads = Hq;
+    f.q_len = Np;
+    f.kv_len = Np;
+    f.ring_p = P;
+    f.bsz = B;
+    f.np = Np;
+    f.causal = p->causal ? 1 : 0;
+    f.scale = eff_scale(p);
+    f.o_bf16 = nullptr;
+    f.o_s_head = d;
+    f.o_s_tok = (int64_t)Hq * d;
+    f.o_s_outer = (int64_t)Np * Hq * d;
+    f.l_s_head = 1;
+    f.l_s_tok = Hq;
+    f.l_s_outer = (int64_t)Np * Hq;
+    f.status = sp;
+
+    for (int t = 0; t < P; ++t) {
+        // causal: rank i attends block i - t only when that block is not in its future
+        f.ring_t = t;
+        f.ring_i0 = f.causal ? t : 0;
+        f.n_outer = (f.causal ? P - t : P) * B;
+        f.o_f32 = t == 0 ? acc_o : part_o;
+        f.lse = t == 0 ? lse : part_l;
+        cudaError_t e = launch_attn_fwd_bf16(f, s);
+        if (e != cudaSuccess) return USP_ERR_CUDA;
+        if (t > 0) {
+            const size_t r0 = (size_t)f.ring_i0 * rows_per_rank;
+            e = launch_lse_merge((int64_t)(rows - r0), d, acc_o + r0 * d, lse + r0, part_o + r0 * d, part_l + r0,
+                                 acc_o + r0 * d, lse + r0, s);
+            if (e != cudaSuccess) return USP_ERR_CUDA;
+        }
+    }
+    return cuda_status(launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s));
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Internal host-side interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Every launcher enqueues on `stream`, returns the
+// launch's cudaError_t and assumes its arguments were validated by api.cu.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace usp {
+
+// ---- all-to-all layout remap (remap.cu)
+// One side is sequence-sharded [P][B][N/P][Hx][d], the other head-sharded
+// [P][B][Hx/P][N][d].  dir 0: seq -> head; dir 1: head -> seq.
+cudaError_t launch_remap(int dir, const void* src, void* dst, int B, int Hx, int N, int P, int row_bytes,
+                         cudaStream_t stream);
+
+// ---- float32 attention forward on CUDA cores (attn_f32.cu)
+// q, o: [Zq][N][d]; k, v: [Zq/g][N][d]; lse: [Zq][N].  Query slot z uses KV slot z/g.
+cudaError_t launch_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int Zq,
+                                int g, int N, int d, int causal, float scale, cudaStream_t stream);
+
+// ---- bf16 tensor-core attention (attn_fwd.cu / attn_bwd.cu)
+// Addressing of one operand family: element (x = column, head, token, outer)
+// sits at x + head*s_head + token*s_tok + outer*s_outer (elements).
+struct Tensor4 {
+    void* ptr;
+    int64_t s_head, s_tok, s_outer;  // strides in elements
+    int n_head, n_tok, n_outer;      // extents
+};
+
+// Work decomposition shared by the Ulysses (head-sharded) and ring
+// (sequence-sharded) forward.  A work item is (q tile, query head, o) with
+// o in [0, n_outer): query rank i = ring_i0 + o/bsz, batch b = o%bsz, KV rank
+// j = (i - ring_t) mod ring_p.  Outer index of q/o/lse: i*bsz + b; of k/v:
+// j*bsz + b.  Token positions: q i*np + token, k/v j*np + token.
+// Head-sharded layout: ring_i0 = ring_t = 0, ring_p = bsz = 1, np = 0, n_outer = 1.
+struct FwdParams {
+    Tensor4 q, k, v;
+    int d;
+    int g;            // query heads per KV head
+    int n_heads;      // query heads per outer index
+    int n_outer;      // outer indices processed by this launch
+    int q_len, kv_len;
+    int ring_i0, ring_t, ring_p, bsz, np;
+    int causal;
+    float scale;
+    // epilogue: o_bf16 (bf16, strides as q) or o_f32 (float32); one is null
+    void* o_bf16;
+    float* o_f32;
+    int64_t o_s_head, o_s_tok, o_s_outer;   // elements
+    float* lse;
+    int64_t l_s_head, l_s_tok, l_s_outer;   // elements
+    int* status;
+};
+cudaError_t launch_attn_fwd_bf16(const FwdParams& p, cudaStream_t stream);
+
+// Backward (head-sharded).  q, o, dout, dq: [Zq][N][d]; k, v, dk, dv: [Zq/g][N][d];
+// lse, dvec: [Zq][N] float32.
+struct BwdParams {
+    const void *q, *k, *v, *o, *dout;
+    const float* lse;
+    float* dvec;  // workspace: D_i = dO_i . O_i
+    void *dq, *dk, *dv;
+    int Zq, g, N, d, causal;
+    float scale;
+    int* status;
+};
+cudaError_t launch_attn_bwd_bf16(const BwdParams& p, cudaStream_t stream);
+
+// ---- ring attention merge (ring.cu)
+cudaError_t launch_lse_merge(int64_t rows, int d, const float* o_a, const float* lse_a, const float* o_b,
+                             const float* lse_b, float* o, float* lse, cudaStream_t stream);
+// fp32 partial -> bf16 output (final ring step)
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t stream);
+// fill float32 buffer with a constant (running LSE starts at -inf)
+cudaError_t launch_fill_f32(float* dst, float value, int64_t n, cudaStream_t stream);
+
+// ---- tensor maps (api.cu)
+// 4-D bf16 tensor map over Tensor4 with box {64, 1, 128, 1} and 128-byte swizzle.
+bool make_tmap_bf16(CUtensorMap* map, const Tensor4& t, int d, int box_rows);
+
+}  // namespace usp

@@ -1,0 +1,180 @@
+/*
+ * usp.h -- C ABI of libusp: Ulysses sequence-parallel attention on one GB300.
+ *
+ * What the library computes (sources are the web pages on Ulysses sequence
+ * parallelism and context parallelism):
+ *  - "Million-Token-Kontexte im Training" (bytewire.ai), section "Ulysses: Die
+ *    Sequenz als Verteilungseinheit": the sequence is split along tokens over
+ *    P devices; for attention, Q, K and V are exchanged by an all-to-all.
+ *  - "Ulysses Sequence Parallelism" (topot.news), section "Как работает
+ *    Ulysses": equal parts per device; after the all-to-all each device has
+ *    the full context for its share of the attention.
+ *  - "Context Parallelism" (ultralytics.com glossary), sections "So
+ *    funktioniert Kontextparallelitaet" (ring attention: partial attention
+ *    per KV block, exact equality with full-sequence attention; token-local
+ *    layers on the local shard) and "Praktische Anwendung und Kompromisse"
+ *    (B x H x N x d tensors with the sequence at dimension 2, causal scaled
+ *    dot product attention, loss mean(out^2) and its backward).
+ *
+ * The P "ranks" are P slices of device buffers on ONE GPU; the all-to-all is
+ * an on-device layout remap.
+ *
+ * Layouts (row-major, innermost last; every tensor is one contiguous device
+ * buffer):
+ *   logical          [B][H][N][d]
+ *   sequence-sharded [P][B][N/P][H][d]   rank p holds tokens [p*N/P, (p+1)*N/P)
+ *   head-sharded     [P][B][H/P][N][d]   rank r holds heads  [r*H/P, (r+1)*H/P)
+ *   LSE (head-sharded attention)    float32 [P][B][Hq/P][N]
+ *   LSE (sequence-sharded ring)     float32 [P][B][N/P][Hq]
+ * H is Hq for Q, O, dO, dQ and Hkv for K, V, dK, dV.  Query head h attends
+ * with KV head h / (Hq/Hkv) (contiguous groups); each rank's query heads then
+ * use only that rank's KV heads.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller allocates and owns every buffer.  The library
+ *    never allocates, frees or synchronises (except usp_device_status, which
+ *    synchronises the given stream to read the status word).
+ *  - Streams: all work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) in call order.  Inputs must stay valid until the
+ *    work completes.
+ *  - Errors: arguments are validated on the host before anything is
+ *    enqueued; a non-OK status means nothing was enqueued.  A launch failure
+ *    returns USP_ERR_CUDA.  Device-side waits are bounded; a wait that gives
+ *    up records USP_ERR_TIMEOUT in a device status word that
+ *    usp_device_status() reads.  No C++ exception crosses this ABI.
+ *  - Pointers: device pointers, 16-byte aligned, non-overlapping unless a
+ *    function says otherwise.  Empty problems (B == 0 or N == 0) are valid
+ *    and enqueue nothing.
+ *  - Precision: USP_BF16 tensors are bf16 with float32 accumulation; the
+ *    softmax probabilities are rounded to bf16 before the P.V product.
+ *    USP_F32 attention runs in true float32 (CUDA cores, forward only).
+ */
+#ifndef USP_H
+#define USP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    USP_OK = 0,
+    USP_ERR_INVALID_ARG = 1, /* null problem, bad sizes or divisibility */
+    USP_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. d not 64/128) */
+    USP_ERR_MISALIGNED = 3,  /* a pointer is NULL or not 16-byte aligned */
+    USP_ERR_WORKSPACE = 4,   /* workspace too small */
+    USP_ERR_CUDA = 5,        /* a CUDA runtime/driver call or launch failed */
+    USP_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
+} usp_status;
+
+typedef enum { USP_F32 = 0, USP_BF16 = 1 } usp_dtype;
+
+/* The problem of the glossary page's example: Q of shape B x Hq x N x d,
+ * K and V of shape B x Hkv x N x d, sequence-parallel degree P, causal flag
+ * (is_causal), softmax scale (0 selects the default 1/sqrt(d)).
+ * Requirements: B, N >= 0; Hq, Hkv, P >= 1; N % P == 0; Hq % Hkv == 0;
+ * Hq % P == 0 and Hkv % P == 0 (every rank gets whole heads); d in {64, 128}
+ * for attention. */
+typedef struct {
+    int B;
+    int Hq;
+    int Hkv;
+    int N;
+    int d;
+    int P;
+    int causal;
+    float scale;
+    int dtype; /* usp_dtype */
+} usp_problem;
+
+typedef void* usp_stream; /* cudaStream_t */
+
+/* All-to-all before attention (bytewire.ai "Ulysses: Die Sequenz als
+ * Verteilungseinheit"; topot.news "Как работает Ulysses"):
+ *   dst[r][b][h'][n][:] = src[n/(N/P)][b][n%(N/P)][r*Hx/P + h'][:]
+ * src: sequence-sharded [P][B][N/P][Hx][d]; dst: head-sharded
+ * [P][B][Hx/P][N][d]; element type p->dtype.  Hx is the head count of the
+ * tensor moved (p->Hq or p->Hkv); Hx % P == 0.  A bit-exact copy.
+ * d * element size must be a multiple of 16 bytes.  src and dst must not
+ * overlap. */
+usp_status usp_a2a_seq2head(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream);
+
+/* All-to-all after attention, the inverse of usp_a2a_seq2head (token-local
+ * layers then run on the local shard: ultralytics.com "So funktioniert"):
+ *   dst[p][b][n'][h][:] = src[h/(Hx/P)][b][h%(Hx/P)][p*N/P + n'][:]
+ * src head-sharded, dst sequence-sharded.  Same rules as above. */
+usp_status usp_a2a_head2seq(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream);
+
+/* Attention forward on head-sharded buffers (every rank, one call):
+ *   S_ij = scale * Q_i . K_j ;  causal: keys j > i are masked
+ *   O_i  = softmax_j(S_i) V ;   lse_i = ln sum_j exp(S_ij)   (float32)
+ * q, o: [P][B][Hq/P][N][d]; k, v: [P][B][Hkv/P][N][d]; lse: [P][B][Hq/P][N].
+ * dtype BF16: tensor cores (d = 64 or 128).  dtype F32: float32 CUDA cores.
+ * ("Context Parallelism", ultralytics.com: scaled_dot_product_attention with
+ * is_causal=True in "Praktische Anwendung und Kompromisse".) */
+usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
+                        float* lse, usp_stream stream);
+
+/* Bytes of workspace usp_attn_bwd needs: linear in N (one float32 per query
+ * row), never quadratic.  Returns 0 for an invalid problem. */
+size_t usp_attn_bwd_workspace_size(const usp_problem* p);
+
+/* Attention backward on head-sharded buffers (the backward of the glossary
+ * page's example, any upstream gradient dO):
+ *   P_ij = exp(S_ij - lse_i);  D_i = dO_i . O_i
+ *   dV_j = sum_{h in group} sum_i P_ij dO_i
+ *   dS_ij = P_ij (dO_i . V_j - D_i)
+ *   dQ_i = scale sum_j dS_ij K_j ;  dK_j = scale sum_{h in group} sum_i dS_ij Q_i
+ * q, o, dout, dq as q above; k, v, dk, dv as k above; lse from usp_attn_fwd.
+ * ws: device workspace of at least usp_attn_bwd_workspace_size(p) bytes,
+ * 256-byte aligned; its contents on entry do not matter.  dtype BF16 only
+ * (USP_ERR_UNSUPPORTED for F32). */
+usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                        size_t ws_bytes, usp_stream stream);
+
+/* Bytes of workspace usp_ring_attn_fwd needs (float32 running output and
+ * LSE plus one float32 partial per query row): linear in N. */
+size_t usp_ring_workspace_size(const usp_problem* p);
+
+/* Ring attention forward on sequence-sharded buffers ("Context
+ * Parallelism", ultralytics.com, "So funktioniert Kontextparallelitaet"):
+ * for step t = 0..P-1 rank i attends KV block j = (i - t) mod P -- skipped
+ * when j > i under the causal mask, masked only when j == i -- and merges the
+ * partial into its running result by log-sum-exp (usp_ring_merge).  Passing
+ * a KV block to the next rank is an index rotation on one GPU.
+ * q, o: [P][B][N/P][Hq][d] bf16; k, v: [P][B][N/P][Hkv][d] bf16;
+ * lse: float32 [P][B][N/P][Hq].  ws: at least usp_ring_workspace_size(p)
+ * bytes, 256-byte aligned.  dtype BF16, d in {64, 128}. */
+usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
+                             float* lse, void* ws, size_t ws_bytes, usp_stream stream);
+
+/* Exact merge of two partial attentions over disjoint key sets, float32
+ * (the merge step of ring attention):
+ *   lse = ln(exp(lse_a) + exp(lse_b))
+ *   o   = exp(lse_a - lse) o_a + exp(lse_b - lse) o_b
+ * A row with lse = -inf is an empty partial and contributes nothing; two
+ * empty rows give lse = -inf and o = 0.
+ * o_*: [rows][d]; lse_*: [rows].  o may alias o_a or o_b and lse may alias
+ * lse_a or lse_b (element-wise, in place).  d >= 1 and d % 4 == 0. */
+usp_status usp_ring_merge(int64_t rows, int d, const float* o_a, const float* lse_a, const float* o_b,
+                          const float* lse_b, float* o, float* lse, usp_stream stream);
+
+/* Synchronises `stream` and reads the device status word that bounded
+ * device-side waits write: USP_OK, or USP_ERR_TIMEOUT (the word is then
+ * cleared).  USP_ERR_CUDA if the synchronisation itself fails. */
+usp_status usp_device_status(usp_stream stream);
+
+/* Static, human-readable name of a status code. */
+const char* usp_status_string(usp_status s);
+
+/* Static build description (architecture, version). */
+const char* usp_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USP_H */

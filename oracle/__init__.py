@@ -64,12 +64,12 @@ def _load():
                                           _vp, _vp, _vp, _c_int]
             lib.orc_attn_bwd_q_rows.restype = _c_int
             lib.orc_attn_bwd_q_rows.argtypes = [_c_int, _c_int, _c_int, _c_long, _c_int, _vp, _vp, _vp,
-                                                _vp, _c_int, _c_int, ctypes.c_double, _c_long, _vp, _vp,
-                                                _c_int]
+                                                _vp, _c_int, _c_int, _c_int, ctypes.c_double, _c_long, _vp,
+                                                _vp, _c_int]
             lib.orc_attn_bwd_kv_rows.restype = _c_int
             lib.orc_attn_bwd_kv_rows.argtypes = [_c_int, _c_int, _c_int, _c_long, _c_int, _vp, _vp, _vp,
-                                                 _vp, _c_int, _c_int, ctypes.c_double, _vp, _vp, _c_long,
-                                                 _vp, _vp, _vp, _c_int]
+                                                 _vp, _c_int, _c_int, _c_int, ctypes.c_double, _vp, _vp,
+                                                 _c_long, _vp, _vp, _vp, _c_int]
             lib.orc_lse_merge.restype = None
             lib.orc_lse_merge.argtypes = [_c_long, _c_int, _vp, _vp, _vp, _vp, _vp, _vp]
             _lib = lib
@@ -158,18 +158,21 @@ def attn_rows(q, k, v, rows=None, causal=True, scale=None, key_lo=0, key_hi=None
 
 
 def attn_bwd_q_rows(q, k, v, dout, rows=None, causal=True, scale=None, nthreads=None):
-    """dQ of the selected query rows for upstream gradient dO, float64 [B][Hq][nrows][d]."""
+    """dQ of the selected query rows for upstream gradient dO, float64 [B][Hq][nrows][d].
+
+    dO may be float32 or bf16 bits independently of Q, K, V.
+    """
     q, k, v, dout = _c(q), _c(k), _c(v), _c(dout)
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
-    if dout.shape != q.shape or dout.dtype != q.dtype:
-        raise ValueError("dO must match Q in shape and dtype")
+    if dout.shape != q.shape:
+        raise ValueError("dO must match Q in shape")
     rows = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     dq = np.empty((B, Hq, len(rows), d), dtype=np.float64)
     rc = _load().orc_attn_bwd_q_rows(B, Hq, Hkv, N, d, q.ctypes.data, k.ctypes.data, v.ctypes.data,
-                                     dout.ctypes.data, _dtype_code(q), int(bool(causal)), scale,
-                                     len(rows), rows.ctypes.data, dq.ctypes.data, nthreads or threads())
+                                     dout.ctypes.data, _dtype_code(q), _dtype_code(dout), int(bool(causal)),
+                                     scale, len(rows), rows.ctypes.data, dq.ctypes.data, nthreads or threads())
     if rc != 0:
         raise ValueError("orc_attn_bwd_q_rows: bad arguments")
     return dq
@@ -194,8 +197,8 @@ def attn_bwd_kv_rows(q, k, v, dout, lse, dvec, rows=None, causal=True, scale=Non
     dk = np.empty((B, Hkv, len(rows), d), dtype=np.float64)
     dv = np.empty((B, Hkv, len(rows), d), dtype=np.float64)
     rc = _load().orc_attn_bwd_kv_rows(B, Hq, Hkv, N, d, q.ctypes.data, k.ctypes.data, v.ctypes.data,
-                                      dout.ctypes.data, _dtype_code(q), int(bool(causal)), scale,
-                                      lse.ctypes.data, dvec.ctypes.data, len(rows), rows.ctypes.data,
+                                      dout.ctypes.data, _dtype_code(q), _dtype_code(dout), int(bool(causal)),
+                                      scale, lse.ctypes.data, dvec.ctypes.data, len(rows), rows.ctypes.data,
                                       dk.ctypes.data, dv.ctypes.data, nthreads or threads())
     if rc != 0:
         raise ValueError("orc_attn_bwd_kv_rows: bad arguments")

@@ -268,10 +268,11 @@ int orc_attn_rows(int B, int Hq, int Hkv, long N, int d, const void* q, const vo
  *   dS_ij = P_ij (dP_ij - D_i)
  *   dQ_i  = scale * sum_j dS_ij K_j
  * dO is the full logical [B][Hq][N][d] tensor (only the selected rows are
- * read).  Output dq [B][Hq][nrows][d].                                      */
+ * read), float32 or bf16 independently of Q/K/V (dout_dtype).  Output dq
+ * [B][Hq][nrows][d].                                      */
 
 typedef struct {
-    int B, Hq, Hkv, d, dtype, causal;
+    int B, Hq, Hkv, d, dtype, dout_dtype, causal;
     long N, nrows;
     double scale;
     const void *q, *k, *v, *dout;
@@ -308,13 +309,13 @@ static void bwdq_item(void* vctx, long item) {
         for (int t = 0; t < d; ++t) oi[t] += s[j] * elem(c->v, c->dtype, vbase + t);
     }
     double Di = 0.0;
-    for (int t = 0; t < d; ++t) Di += elem(c->dout, c->dtype, qbase + t) * oi[t];
+    for (int t = 0; t < d; ++t) Di += elem(c->dout, c->dout_dtype, qbase + t) * oi[t];
     double* dqrow = c->dq + ((size_t)bh * c->nrows + r) * d;
     for (int t = 0; t < d; ++t) dqrow[t] = 0.0;
     for (long j = 0; j < jhi; ++j) {
         size_t vbase = (((size_t)b * c->Hkv + hk) * c->N + j) * d;
         double dp = 0.0;
-        for (int t = 0; t < d; ++t) dp += elem(c->dout, c->dtype, qbase + t) * elem(c->v, c->dtype, vbase + t);
+        for (int t = 0; t < d; ++t) dp += elem(c->dout, c->dout_dtype, qbase + t) * elem(c->v, c->dtype, vbase + t);
         double ds = s[j] * (dp - Di);
         for (int t = 0; t < d; ++t) dqrow[t] += c->scale * ds * elem(c->k, c->dtype, vbase + t);
     }
@@ -323,12 +324,12 @@ static void bwdq_item(void* vctx, long item) {
 }
 
 int orc_attn_bwd_q_rows(int B, int Hq, int Hkv, long N, int d, const void* q, const void* k, const void* v,
-                        const void* dout, int dtype, int causal, double scale, long nrows,
+                        const void* dout, int dtype, int dout_dtype, int causal, double scale, long nrows,
                         const int64_t* rows, double* dq, int nthreads) {
     if (Hkv < 1 || Hq % Hkv != 0 || nrows < 0) return 1;
     for (long r = 0; r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= N) return 1;
-    bwdq_ctx c = {B, Hq, Hkv, d, dtype, causal, N, nrows, scale, q, k, v, dout, rows, dq};
+    bwdq_ctx c = {B, Hq, Hkv, d, dtype, dout_dtype, causal, N, nrows, scale, q, k, v, dout, rows, dq};
     parallel_for(bwdq_item, &c, (long)B * Hq * nrows, nthreads);
     return 0;
 }
@@ -346,7 +347,7 @@ int orc_attn_bwd_q_rows(int B, int Hq, int Hkv, long N, int d, const void* q, co
  * Outputs dk, dv: [B][Hkv][nrows][d].                                      */
 
 typedef struct {
-    int B, Hq, Hkv, d, dtype, causal;
+    int B, Hq, Hkv, d, dtype, dout_dtype, causal;
     long N, nrows;
     double scale;
     const void *q, *k, *v, *dout;
@@ -377,10 +378,10 @@ static void bwdkv_item(void* vctx, long item) {
             double lse_i = c->lse[((size_t)b * c->Hq + h) * c->N + i];
             double pij = exp(sij - lse_i);
             double dp = 0.0;
-            for (int t = 0; t < d; ++t) dp += elem(c->dout, c->dtype, qbase + t) * elem(c->v, c->dtype, kbase + t);
+            for (int t = 0; t < d; ++t) dp += elem(c->dout, c->dout_dtype, qbase + t) * elem(c->v, c->dtype, kbase + t);
             double ds = pij * (dp - c->dvec[((size_t)b * c->Hq + h) * c->N + i]);
             for (int t = 0; t < d; ++t) {
-                dvrow[t] += pij * elem(c->dout, c->dtype, qbase + t);
+                dvrow[t] += pij * elem(c->dout, c->dout_dtype, qbase + t);
                 dkrow[t] += c->scale * ds * elem(c->q, c->dtype, qbase + t);
             }
         }
@@ -388,13 +389,13 @@ static void bwdkv_item(void* vctx, long item) {
 }
 
 int orc_attn_bwd_kv_rows(int B, int Hq, int Hkv, long N, int d, const void* q, const void* k, const void* v,
-                         const void* dout, int dtype, int causal, double scale, const double* lse,
+                         const void* dout, int dtype, int dout_dtype, int causal, double scale, const double* lse,
                          const double* dvec, long nrows, const int64_t* rows, double* dk, double* dv,
                          int nthreads) {
     if (Hkv < 1 || Hq % Hkv != 0 || nrows < 0) return 1;
     for (long r = 0; r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= N) return 1;
-    bwdkv_ctx c = {B, Hq, Hkv, d, dtype, causal, N, nrows, scale, q, k, v, dout, lse, dvec, rows, dk, dv};
+    bwdkv_ctx c = {B, Hq, Hkv, d, dtype, dout_dtype, causal, N, nrows, scale, q, k, v, dout, lse, dvec, rows, dk, dv};
     parallel_for(bwdkv_item, &c, (long)B * Hkv * nrows, nthreads);
     return 0;
 }

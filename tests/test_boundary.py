@@ -1,0 +1,133 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+symbol include/usp.h declares, and rejects bad arguments on the host before
+any CUDA call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import context_long_attention_ulysses_gb300 as usp
+from context_long_attention_ulysses_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "usp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(usp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert _declared() == sorted(_lib.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert usp.usp_status_string(0) == "USP_OK"
+    assert usp.usp_status_string(6) == "USP_ERR_TIMEOUT"
+    assert usp.usp_status_string(99) == "USP_ERR_UNKNOWN"
+    assert "sm_103a" in usp.usp_build_info()
+
+
+def _p(**kw):
+    base = dict(B=1, Hq=4, Hkv=4, N=256, d=64, P=2, causal=True, scale=0.0, dtype="bf16")
+    base.update(kw)
+    return usp.Problem(**base)
+
+
+FAKE = 1 << 20  # 16-byte aligned fake device address; never dereferenced here
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=255), _lib.USP_ERR_INVALID_ARG),          # N % P
+    (dict(Hq=6, Hkv=4), _lib.USP_ERR_INVALID_ARG),    # Hq % Hkv
+    (dict(Hq=3, Hkv=3), _lib.USP_ERR_INVALID_ARG),    # Hq % P
+    (dict(Hq=4, Hkv=1), _lib.USP_ERR_INVALID_ARG),    # Hkv % P
+    (dict(P=0), _lib.USP_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.USP_ERR_INVALID_ARG),
+    (dict(scale=-1.0), _lib.USP_ERR_INVALID_ARG),
+    (dict(d=96), _lib.USP_ERR_UNSUPPORTED),           # attention only for d in {64, 128}
+])
+def test_attention_argument_errors(lib, kw, code):
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_attn_fwd(_p(**kw), FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert e.value.status == code
+
+
+def test_null_problem_and_pointers(lib):
+    assert lib.usp_attn_fwd(None, FAKE, FAKE, FAKE, FAKE, FAKE, None) == _lib.USP_ERR_INVALID_ARG
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_attn_fwd(_p(), FAKE, 0, FAKE, FAKE, FAKE)
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_a2a_seq2head(_p(), 4, FAKE + 8, FAKE * 2)
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+
+
+def test_remap_argument_errors(lib):
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_a2a_seq2head(_p(), 3, FAKE, FAKE * 2)       # Hx is neither Hq nor Hkv
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_a2a_seq2head(_p(d=48), 4, FAKE, FAKE * 2)   # 96-byte rows
+    assert e.value.status == _lib.USP_ERR_UNSUPPORTED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_a2a_head2seq(_p(), 4, FAKE, FAKE + 4096)    # overlapping buffers
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+
+
+def test_backward_and_ring_argument_errors(lib):
+    p = _p()
+    ws = usp.usp_attn_bwd_workspace_size(p)
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_attn_bwd(p, *([FAKE] * 9), FAKE, ws - 256)
+    assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_attn_bwd(p, *([FAKE] * 9), FAKE + 16, ws)   # workspace must be 256-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_attn_bwd(_p(dtype="f32"), *([FAKE] * 9), FAKE, ws)
+    assert e.value.status == _lib.USP_ERR_UNSUPPORTED
+    rws = usp.usp_ring_workspace_size(p)
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_ring_attn_fwd(p, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, rws - 1)
+    assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_ring_merge(10, 6, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)   # d % 4
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+
+
+def test_empty_problems_enqueue_nothing(lib):
+    # B == 0 or N == 0 is valid and returns before any CUDA call
+    for kw in (dict(N=0), dict(B=0)):
+        p = _p(**kw)
+        usp.usp_a2a_seq2head(p, 4, 0, 0)
+        usp.usp_attn_fwd(p, 0, 0, 0, 0, 0)
+        usp.usp_attn_bwd(p, *([0] * 9), 0, 0)
+        usp.usp_ring_attn_fwd(p, 0, 0, 0, 0, 0, 0, 0)
+    usp.usp_ring_merge(0, 64, 0, 0, 0, 0, 0, 0)
+
+
+def test_workspaces_are_linear_in_sequence_length(lib):
+    for N in (1024, 4096, 131072):
+        a = usp.usp_attn_bwd_workspace_size(_p(N=N, Hq=32, Hkv=8, d=128, P=8))
+        b = usp.usp_attn_bwd_workspace_size(_p(N=2 * N, Hq=32, Hkv=8, d=128, P=8))
+        assert b == 2 * a
+        assert a == 2 * 4 * 32 * N  # D_i and lse_i*log2(e), float32, per query row
+        r1 = usp.usp_ring_workspace_size(_p(N=N, Hq=32, Hkv=32, d=128, P=8))
+        r2 = usp.usp_ring_workspace_size(_p(N=2 * N, Hq=32, Hkv=32, d=128, P=8))
+        assert r2 == 2 * r1
+    assert usp.usp_attn_bwd_workspace_size(_p(N=255)) == 0  # invalid problem

@@ -1,0 +1,212 @@
+"""GPU parity of the CUDA path (through the C ABI) against the float64 oracle,
+at sizes the oracle finishes in seconds: every element compared."""
+import numpy as np
+import pytest
+
+from tests.helpers import (TOL_BF16_GRAD_RELFRO, TOL_BF16_O_MAXABS, TOL_BF16_O_RELFRO, TOL_F32_MAXABS, TOL_LSE_BF16,
+                           TOL_LSE_F32, f64, from_head, from_seq, gen, max_abs, rel_fro, to_dev, to_head, to_host,
+                           to_seq)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def usp():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import context_long_attention_ulysses_gb300 as m
+    from context_long_attention_ulysses_gb300 import build
+    build.build()
+    return m
+
+
+def _sync():
+    import torch
+    torch.cuda.synchronize()
+
+
+def _status_ok(usp):
+    assert usp.usp_device_status() == 0
+
+
+# ---------------------------------------------------------------- remaps
+@pytest.mark.parametrize("dtype,B,H,N,d,P", [
+    ("f32", 1, 4, 256, 64, 2), ("bf16", 1, 4, 4096, 64, 2), ("bf16", 2, 8, 1000, 128, 4),
+    ("bf16", 1, 32, 2048, 128, 8), ("f32", 3, 6, 96, 128, 3), ("bf16", 1, 8, 64, 32, 8)])
+def test_remap_bit_exact(usp, orc, dtype, B, H, N, d, P):
+    import torch
+    p = usp.Problem(B=B, Hq=H, Hkv=H, N=N, d=d, P=P, dtype=dtype)
+    x = gen((B, H, N, d), 0, dtype)
+    seq = to_seq(x, P)
+    src = to_dev(seq, dtype)
+    head = torch.empty(p.head_shape(H), dtype=p.torch_dtype, device="cuda")
+    back = torch.empty_like(src)
+    usp.usp_a2a_seq2head(p, H, src, head)
+    usp.usp_a2a_head2seq(p, H, head, back)
+    _sync()
+    want = orc.seq2head(seq)
+    got = to_host(head)
+    assert got.tobytes() == want.tobytes()
+    assert to_host(back).tobytes() == seq.tobytes()
+    _status_ok(usp)
+
+
+# ---------------------------------------------------------------- tiny fp32 case
+def test_tiny_exactness_case_fp32(usp, orc):
+    """B=1, H=4, N=256, d=64, fp32, causal, P=2: remap -> attention -> remap, in full."""
+    B, H, N, d, P = 1, 4, 256, 64, 2
+    p = usp.Problem(B=B, Hq=H, Hkv=H, N=N, d=d, P=P, dtype="f32")
+    q, k, v = (gen((B, H, N, d), s, "f32") for s in (0, 1, 2))
+    o_seq, saved = usp.ulysses_attention_fwd(p, to_dev(to_seq(q, P), "f32"), to_dev(to_seq(k, P), "f32"),
+                                             to_dev(to_seq(v, P), "f32"))
+    _sync()
+    # the all-to-all results are the oracle's, bit for bit
+    assert to_host(saved["q"]).tobytes() == orc.seq2head(to_seq(q, P)).tobytes()
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=True)
+    o = from_seq(to_host(o_seq))
+    assert max_abs(o, o_ref) < TOL_F32_MAXABS
+    assert max_abs(from_head(to_host(saved["lse"])), lse_ref) < TOL_LSE_F32
+    _status_ok(usp)
+
+
+# ---------------------------------------------------------------- bf16 fwd + bwd
+def _ulysses_fwd_bwd(usp, B, Hq, Hkv, N, d, P, causal, dO=None):
+    import torch
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P, causal=causal)
+    q, k, v = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2)
+    o_seq, saved = usp.ulysses_attention_fwd(p, to_dev(to_seq(q, P)), to_dev(to_seq(k, P)), to_dev(to_seq(v, P)))
+    if dO is None:  # loss = mean(out.float()^2): dO = 2 O / numel, formed in float32 and rounded to bf16
+        do_seq = (2.0 * o_seq.float() / o_seq.numel()).to(torch.bfloat16)
+    else:
+        do_seq = to_dev(to_seq(dO, P))
+    dq, dk, dv = usp.ulysses_attention_bwd(p, saved, do_seq)
+    _sync()
+    out = dict(o=from_seq(to_host(o_seq)), lse=from_head(to_host(saved["lse"])), dq=from_seq(to_host(dq)),
+               dk=from_seq(to_host(dk)), dv=from_seq(to_host(dv)))
+    return (q, k, v), out
+
+
+def _check_fwd(o, lse, o_ref, lse_ref):
+    assert max_abs(f64(o), o_ref) < TOL_BF16_O_MAXABS
+    assert rel_fro(f64(o), o_ref) < TOL_BF16_O_RELFRO
+    assert max_abs(lse, lse_ref) < TOL_LSE_BF16
+
+
+def _check_grads(out, dq, dk, dv):
+    for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+        err = rel_fro(f64(out[name]), ref)
+        assert err < TOL_BF16_GRAD_RELFRO, (name, err)
+
+
+def test_example_shape_fwd_bwd_mean_square_loss(usp, orc):
+    """The glossary page's example: B=1, H=4, N=4096, d=64, bf16, causal, P=2, loss mean(out^2)."""
+    B, H, N, d, P = 1, 4, 4096, 64, 2
+    (q, k, v), out = _ulysses_fwd_bwd(usp, B, H, H, N, d, P, True)
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=True)
+    _check_fwd(out["o"], out["lse"], o_ref, lse_ref)
+    # the oracle's own loss gradient, from its own output
+    dO_ref = (2.0 * o_ref / o_ref.size).astype(np.float32)
+    dq, dk, dv, _, _ = orc.attn_bwd_full(q, k, v, dO_ref, causal=True)
+    _check_grads(out, dq, dk, dv)
+    _status_ok(usp)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,P,causal", [
+    (1, 8, 2, 1000, 128, 2, True),     # GQA, ragged tail (N not a multiple of 128)
+    (2, 4, 4, 520, 64, 2, True),       # two sequences, ragged
+    (1, 4, 2, 384, 128, 2, False),     # full (non-causal) attention
+    (1, 2, 1, 200, 64, 1, True),       # one rank: no exchange at all
+    (1, 8, 8, 130, 128, 2, True),      # one full tile plus a 2-row tail per head
+])
+def test_fwd_bwd_edge_cases(usp, orc, B, Hq, Hkv, N, d, P, causal):
+    dO = gen((B, Hq, N, d), 3)
+    (q, k, v), out = _ulysses_fwd_bwd(usp, B, Hq, Hkv, N, d, P, causal, dO)
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=causal)
+    _check_fwd(out["o"], out["lse"], o_ref, lse_ref)
+    dq, dk, dv, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
+    _check_grads(out, dq, dk, dv)
+    _status_ok(usp)
+
+
+def test_sharded_equals_unsharded_bitwise(usp):
+    """Sharded attention is the same per-head work as one unsharded pass: bit-identical."""
+    import torch
+    B, Hq, Hkv, N, d = 1, 8, 4, 768, 128
+    q, k, v = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2)
+    outs = []
+    for P in (1, 4):
+        p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P)
+        o_seq, saved = usp.ulysses_attention_fwd(p, to_dev(to_seq(q, P)), to_dev(to_seq(k, P)), to_dev(to_seq(v, P)))
+        torch.cuda.synchronize()
+        outs.append((from_seq(to_host(o_seq)), from_head(to_host(saved["lse"]))))
+    assert outs[0][0].tobytes() == outs[1][0].tobytes()
+    assert outs[0][1].tobytes() == outs[1][1].tobytes()
+
+
+def test_rank_reads_only_its_own_buffers(usp):
+    """Poison one rank's query heads with NaN: every other rank's output is unchanged."""
+    import torch
+    B, Hq, Hkv, N, d, P = 1, 8, 4, 512, 64, 4
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P)
+    q, k, v = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2)
+    qh, kh, vh = to_dev(to_head(q, P)), to_dev(to_head(k, P)), to_dev(to_head(v, P))
+    o1 = torch.empty_like(qh)
+    l1 = torch.empty(p.lse_head_shape(), dtype=torch.float32, device="cuda")
+    usp.usp_attn_fwd(p, qh, kh, vh, o1, l1)
+    qh2 = qh.clone()
+    qh2[2] = float("nan")
+    kh2 = kh.clone()
+    kh2[1] = float("nan")
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    usp.usp_attn_fwd(p, qh2, kh2, vh, o2, l2)
+    torch.cuda.synchronize()
+    for r in range(P):
+        if r in (1, 2):
+            assert torch.isnan(o2[r].float()).all()
+        else:
+            assert torch.equal(o1[r], o2[r]) and torch.equal(l1[r], l2[r])
+
+
+# ---------------------------------------------------------------- ring mode
+def test_lse_merge_kernel(usp, orc):
+    import torch
+    rows, d = 3000, 128
+    rng = np.random.default_rng(5)
+    oa, ob = rng.standard_normal((2, rows, d)).astype(np.float32)
+    la, lb = (rng.standard_normal((2, rows)) * 4).astype(np.float32)
+    la[::7] = -np.inf
+    lb[::11] = -np.inf
+    lb[::77] = -np.inf  # both empty on rows divisible by 77
+    la[::77] = -np.inf
+    oa[::7] = np.nan    # an empty partial's output must not leak
+    ref_o, ref_l = orc.lse_merge(np.nan_to_num(oa), la, ob, lb)
+    t = [torch.from_numpy(x).cuda() for x in (oa, la, ob, lb)]
+    o = torch.empty_like(t[0])
+    lse = torch.empty_like(t[1])
+    usp.usp_ring_merge(rows, d, t[0], t[1], t[2], t[3], o, lse)
+    # in place into the first operand
+    usp.usp_ring_merge(rows, d, t[0], t[1], t[2], t[3], t[0], t[1])
+    torch.cuda.synchronize()
+    for oo, ll in ((o, lse), (t[0], t[1])):
+        assert max_abs(oo.cpu().numpy(), ref_o) < 1e-5
+        lh = ll.cpu().numpy()
+        assert np.array_equal(np.isinf(lh), np.isinf(ref_l))
+        fin = np.isfinite(ref_l)
+        assert max_abs(lh[fin], ref_l[fin]) < 1e-5
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,P,causal", [
+    (1, 4, 4, 2048, 128, 4, True), (1, 4, 2, 1536, 64, 3, True), (2, 2, 2, 1000, 128, 2, True),
+    (1, 4, 4, 1024, 128, 4, False)])
+def test_ring_attention_small(usp, orc, B, H, Hkv, N, d, P, causal):
+    import torch
+    p = usp.Problem(B=B, Hq=H, Hkv=Hkv, N=N, d=d, P=P, causal=causal)
+    q, k, v = gen((B, H, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2)
+    o, lse = usp.ring_attention_fwd(p, to_dev(to_seq(q, P)), to_dev(to_seq(k, P)), to_dev(to_seq(v, P)))
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=causal)
+    o_log = from_seq(to_host(o))
+    lse_log = np.ascontiguousarray(to_host(lse).transpose(1, 3, 0, 2).reshape(B, H, N))
+    _check_fwd(o_log, lse_log, o_ref, lse_ref)
+    _status_ok(usp)
