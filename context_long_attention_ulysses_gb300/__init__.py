@@ -19,13 +19,14 @@ from dataclasses import dataclass
 
 import torch
 
-from ._lib import (SYMBOLS, USP_BF16, USP_F32, USP_OK, UspError, UspProblem, check, load)  # noqa: F401
+from ._lib import (SYMBOLS, USP_BF16, USP_F32, USP_OK, UspError, UspProblem, UspTraceEntry, check,  # noqa: F401
+                   load)
 
 __all__ = [
     "Problem", "UspError", "SYMBOLS",
     "usp_a2a_seq2head", "usp_a2a_head2seq", "usp_attn_fwd", "usp_attn_bwd_workspace_size", "usp_attn_bwd",
     "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
-    "usp_build_info", "ulysses_attention_fwd", "ulysses_attention_bwd", "ring_attention_fwd", "library_path",
+    "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "ulysses_attention_fwd", "ulysses_attention_bwd", "ring_attention_fwd", "library_path",
 ]
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -158,6 +159,25 @@ def usp_status_string(s: int) -> str:
 
 def usp_build_info() -> str:
     return load().usp_build_info().decode()
+
+
+def usp_trace_enable(on: bool = True) -> None:
+    check("usp_trace_enable", load().usp_trace_enable(1 if on else 0))
+
+
+def usp_trace_reset() -> None:
+    check("usp_trace_reset", load().usp_trace_reset())
+
+
+def usp_trace_report() -> dict:
+    """{kernel name: (launches, total milliseconds)} accumulated since the last reset."""
+    lib = load()
+    n = lib.usp_trace_report(None, 0)
+    if n < 0:
+        raise UspError("usp_trace_report", n, "event failure")
+    buf = (UspTraceEntry * max(n, 1))()
+    n = lib.usp_trace_report(buf, n)
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n)}
 
 
 # ------------------------------------------------------------ layer helpers

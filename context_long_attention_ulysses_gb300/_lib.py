@@ -26,7 +26,7 @@ USP_BF16 = 1
 SYMBOLS = (
     "usp_a2a_seq2head", "usp_a2a_head2seq", "usp_attn_fwd", "usp_attn_bwd_workspace_size", "usp_attn_bwd",
     "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
-    "usp_build_info",
+    "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report",
 )
 
 
@@ -35,6 +35,11 @@ class UspProblem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("N", ctypes.c_int),
                 ("d", ctypes.c_int), ("P", ctypes.c_int), ("causal", ctypes.c_int), ("scale", ctypes.c_float),
                 ("dtype", ctypes.c_int)]
+
+
+class UspTraceEntry(ctypes.Structure):
+    """Mirror of ``usp_trace_entry``."""
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
 
 class UspError(RuntimeError):
@@ -75,6 +80,9 @@ def load() -> ctypes.CDLL:
             "usp_device_status": (ci, [vp]),
             "usp_status_string": (ctypes.c_char_p, [ci]),
             "usp_build_info": (ctypes.c_char_p, []),
+            "usp_trace_enable": (ci, [ci]),
+            "usp_trace_reset": (ci, []),
+            "usp_trace_report": (ci, [ctypes.POINTER(UspTraceEntry), ci]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

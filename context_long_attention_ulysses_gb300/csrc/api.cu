@@ -3,7 +3,10 @@
 // out; the library never allocates device memory.
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -52,12 +55,14 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 
 int elem_size(int dtype) { return dtype == USP_F32 ? 4 : (dtype == USP_BF16 ? 2 : 0); }
 
-// Sizes and divisibility shared by every problem-based entry point.
-usp_status check_problem(const usp_problem* p) {
+// Sizes and divisibility shared by every problem-based entry point.  The
+// Ulysses path splits heads over ranks (Hq, Hkv divisible by P); ring mode
+// keeps every head on every rank and only splits tokens.
+usp_status check_problem(const usp_problem* p, bool split_heads = true) {
     if (!p) return USP_ERR_INVALID_ARG;
     if (p->B < 0 || p->N < 0 || p->Hq < 1 || p->Hkv < 1 || p->P < 1) return USP_ERR_INVALID_ARG;
-    if (p->N % p->P != 0 || p->Hq % p->Hkv != 0 || p->Hq % p->P != 0 || p->Hkv % p->P != 0)
-        return USP_ERR_INVALID_ARG;
+    if (p->N % p->P != 0 || p->Hq % p->Hkv != 0) return USP_ERR_INVALID_ARG;
+    if (split_heads && (p->Hq % p->P != 0 || p->Hkv % p->P != 0)) return USP_ERR_INVALID_ARG;
     if (p->dtype != USP_F32 && p->dtype != USP_BF16) return USP_ERR_INVALID_ARG;
     if (p->d < 1) return USP_ERR_INVALID_ARG;
     if (!(p->scale >= 0.f) || std::isinf(p->scale)) return USP_ERR_INVALID_ARG;
@@ -70,6 +75,50 @@ float eff_scale(const usp_problem* p) { return p->scale == 0.f ? 1.0f / std::sqr
 bool empty(const usp_problem* p) { return p->B == 0 || p->N == 0; }
 
 usp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? USP_OK : USP_ERR_CUDA; }
+
+// ---------------------------------------------------------------- tracing
+// When enabled, every kernel launch is bracketed by two CUDA events on its
+// stream; usp_trace_report() resolves them into per-kernel totals.
+struct TraceSlot {
+    const char* name;
+    cudaEvent_t a, b;
+};
+struct TraceAcc {
+    int64_t launches = 0;
+    double ms = 0.0;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceSlot> g_trace_pending;
+std::vector<cudaEvent_t> g_trace_pool;
+std::map<std::string, TraceAcc> g_trace_acc;
+
+cudaEvent_t trace_event() {
+    if (!g_trace_pool.empty()) {
+        cudaEvent_t e = g_trace_pool.back();
+        g_trace_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+template <class F>
+cudaError_t traced(const char* name, cudaStream_t s, F&& launch) {
+    std::unique_lock<std::mutex> lock(g_trace_mu);
+    if (!g_trace_on) {
+        lock.unlock();
+        return launch();
+    }
+    cudaEvent_t a = trace_event(), b = trace_event();
+    if (!a || !b) return cudaErrorMemoryAllocation;
+    cudaEventRecord(a, s);
+    cudaError_t e = launch();
+    cudaEventRecord(b, s);
+    g_trace_pending.push_back({name, a, b});
+    return e;
+}
 
 }  // namespace
 
@@ -130,10 +179,13 @@ static usp_status a2a(int dir, const usp_problem* p, int Hx, const void* src, vo
     if (empty(p)) return USP_OK;
     if (!aligned16(src) || !aligned16(dst)) return USP_ERR_MISALIGNED;
     const size_t bytes = (size_t)p->B * Hx * (size_t)p->N * row_bytes;
-    const char* s = static_cast<const char*>(src);
-    const char* t = static_cast<const char*>(dst);
-    if (s < t + bytes && t < s + bytes) return USP_ERR_INVALID_ARG;  // overlap
-    return cuda_status(launch_remap(dir, src, dst, p->B, Hx, p->N, p->P, row_bytes, static_cast<cudaStream_t>(stream)));
+    const char* sb = static_cast<const char*>(src);
+    const char* tb = static_cast<const char*>(dst);
+    if (sb < tb + bytes && tb < sb + bytes) return USP_ERR_INVALID_ARG;  // overlap
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(traced(dir == 0 ? "a2a_seq2head" : "a2a_head2seq", s, [&] {
+        return launch_remap(dir, src, dst, p->B, Hx, p->N, p->P, row_bytes, s);
+    }));
 }
 
 usp_status usp_a2a_seq2head(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
@@ -192,13 +244,15 @@ usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, cons
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Zq = p->B * p->Hq;
     if (p->dtype == USP_F32)
-        return cuda_status(launch_attn_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                               static_cast<const float*>(v), static_cast<float*>(o), lse, Zq,
-                                               p->Hq / p->Hkv, p->N, p->d, p->causal ? 1 : 0, eff_scale(p), s));
+        return cuda_status(traced("attn_fwd_f32", s, [&] {
+            return launch_attn_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                       static_cast<const float*>(v), static_cast<float*>(o), lse, Zq, p->Hq / p->Hkv,
+                                       p->N, p->d, p->causal ? 1 : 0, eff_scale(p), s);
+        }));
     int* sp = status_ptr();
     if (!sp) return USP_ERR_CUDA;
     FwdParams f = head_sharded_fwd(p, q, k, v, o, lse, sp);
-    return cuda_status(launch_attn_fwd_bf16(f, s));
+    return cuda_status(traced("attn_fwd", s, [&] { return launch_attn_fwd_bf16(f, s); }));
 }
 
 size_t usp_attn_bwd_workspace_size(const usp_problem* p) {
@@ -234,7 +288,11 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
     b.causal = p->causal ? 1 : 0;
     b.scale = eff_scale(p);
     b.status = sp;
-    return cuda_status(launch_attn_bwd_bf16(b, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = traced("attn_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
+    if (e == cudaSuccess) e = traced("attn_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+    if (e == cudaSuccess) e = traced("attn_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
+    return cuda_status(e);
 }
 
 usp_status usp_ring_merge(int64_t rows, int d, const float* o_a, const float* lse_a, const float* o_b,
@@ -244,7 +302,9 @@ usp_status usp_ring_merge(int64_t rows, int d, const float* o_a, const float* ls
     const void* ptrs[] = {o_a, lse_a, o_b, lse_b, o, lse};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
-    return cuda_status(launch_lse_merge(rows, d, o_a, lse_a, o_b, lse_b, o, lse, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(
+        traced("ring_merge", s, [&] { return launch_lse_merge(rows, d, o_a, lse_a, o_b, lse_b, o, lse, s); }));
 }
 
 // Ring workspace: float32 running output [rows][d], float32 partial output
@@ -253,14 +313,14 @@ usp_status usp_ring_merge(int64_t rows, int d, const float* o_a, const float* ls
 static size_t ring_part(size_t bytes) { return (bytes + 255) & ~(size_t)255; }
 
 size_t usp_ring_workspace_size(const usp_problem* p) {
-    if (check_problem(p) != USP_OK) return 0;
+    if (check_problem(p, false) != USP_OK) return 0;
     const size_t rows = (size_t)p->B * p->N * p->Hq;
     return 2 * ring_part(rows * p->d * sizeof(float)) + ring_part(rows * sizeof(float));
 }
 
 usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o, float* lse,
                              void* ws, size_t ws_bytes, usp_stream stream) {
-    usp_status st = check_problem(p);
+    usp_status st = check_problem(p, false);
     if (st != USP_OK) return st;
     if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
     if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
@@ -311,16 +371,64 @@ usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k,
         f.n_outer = (f.causal ? P - t : P) * B;
         f.o_f32 = t == 0 ? acc_o : part_o;
         f.lse = t == 0 ? lse : part_l;
-        cudaError_t e = launch_attn_fwd_bf16(f, s);
+        cudaError_t e = traced("ring_attn_partial", s, [&] { return launch_attn_fwd_bf16(f, s); });
         if (e != cudaSuccess) return USP_ERR_CUDA;
         if (t > 0) {
             const size_t r0 = (size_t)f.ring_i0 * rows_per_rank;
-            e = launch_lse_merge((int64_t)(rows - r0), d, acc_o + r0 * d, lse + r0, part_o + r0 * d, part_l + r0,
-                                 acc_o + r0 * d, lse + r0, s);
+            e = traced("ring_merge", s, [&] {
+                return launch_lse_merge((int64_t)(rows - r0), d, acc_o + r0 * d, lse + r0, part_o + r0 * d,
+                                        part_l + r0, acc_o + r0 * d, lse + r0, s);
+            });
             if (e != cudaSuccess) return USP_ERR_CUDA;
         }
     }
-    return cuda_status(launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s));
+    return cuda_status(traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s); }));
+}
+
+usp_status usp_trace_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    g_trace_on = on != 0;
+    return USP_OK;
+}
+
+usp_status usp_trace_reset(void) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    for (auto& t : g_trace_pending) {
+        cudaEventSynchronize(t.b);
+        g_trace_pool.push_back(t.a);
+        g_trace_pool.push_back(t.b);
+    }
+    g_trace_pending.clear();
+    g_trace_acc.clear();
+    return USP_OK;
+}
+
+int usp_trace_report(usp_trace_entry* out, int max_entries) {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    bool failed = false;
+    for (auto& t : g_trace_pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(t.b) != cudaSuccess || cudaEventElapsedTime(&ms, t.a, t.b) != cudaSuccess)
+            failed = true;
+        TraceAcc& acc = g_trace_acc[t.name];
+        acc.launches += 1;
+        acc.ms += ms;
+        g_trace_pool.push_back(t.a);
+        g_trace_pool.push_back(t.b);
+    }
+    g_trace_pending.clear();
+    if (failed) return -1;
+    int n = 0;
+    for (const auto& kv : g_trace_acc) {
+        if (out && n < max_entries) {
+            std::memset(out[n].name, 0, sizeof(out[n].name));
+            std::strncpy(out[n].name, kv.first.c_str(), sizeof(out[n].name) - 1);
+            out[n].launches = kv.second.launches;
+            out[n].total_ms = kv.second.ms;
+        }
+        ++n;
+    }
+    return n;
 }
 
 }  // extern "C"

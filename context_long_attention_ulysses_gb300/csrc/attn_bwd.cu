@@ -569,28 +569,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+struct BwdMaps {
+    CUtensorMap q, dout, k, v;
+};
+
 template <int D>
-cudaError_t launch_bwd_t(const BwdParams& b, cudaStream_t stream) {
-    const int Npad = (b.N + 127) / 128 * 128;
-    float* dvec = b.dvec;
-    float* lse2 = b.dvec + (size_t)b.Zq * Npad;
-    {
-        const int64_t rows = (int64_t)b.Zq * Npad;
-        bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-            static_cast<const uint16_t*>(b.o), static_cast<const uint16_t*>(b.dout), b.lse, dvec, lse2, b.Zq, b.N, Npad);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
+bool make_bwd_maps(const BwdParams& b, int q_rows, BwdMaps* m) {
     const int Zk = b.Zq / b.g;
     const int64_t nd = (int64_t)b.N * D;
     Tensor4 tq{const_cast<void*>(b.q), nd, D, nd * b.Zq, b.Zq, b.N, 1};
     Tensor4 tdo{const_cast<void*>(b.dout), nd, D, nd * b.Zq, b.Zq, b.N, 1};
     Tensor4 tk{const_cast<void*>(b.k), nd, D, nd * Zk, Zk, b.N, 1};
     Tensor4 tv{const_cast<void*>(b.v), nd, D, nd * Zk, Zk, b.N, 1};
-    CUtensorMap mq64, mdo64, mq128, mdo128, mk, mv;
-    if (!make_tmap_bf16(&mq64, tq, D, 64) || !make_tmap_bf16(&mdo64, tdo, D, 64) || !make_tmap_bf16(&mq128, tq, D, 128) ||
-        !make_tmap_bf16(&mdo128, tdo, D, 128) || !make_tmap_bf16(&mk, tk, D, 128) || !make_tmap_bf16(&mv, tv, D, 128))
-        return cudaErrorInvalidValue;
+    return make_tmap_bf16(&m->q, tq, D, q_rows) && make_tmap_bf16(&m->dout, tdo, D, q_rows) &&
+           make_tmap_bf16(&m->k, tk, D, 128) && make_tmap_bf16(&m->v, tv, D, 128);
+}
+
+DevBwd dev_params(const BwdParams& b) {
+    const int Npad = (b.N + 127) / 128 * 128;
     DevBwd p;
     p.Zq = b.Zq;
     p.g = b.g;
@@ -599,39 +595,60 @@ cudaError_t launch_bwd_t(const BwdParams& b, cudaStream_t stream) {
     p.causal = b.causal;
     p.scale = b.scale;
     p.scale_log2 = b.scale * kLog2e;
-    p.lse2 = lse2;
-    p.dvec = dvec;
+    p.dvec = b.dvec;
+    p.lse2 = b.dvec + (size_t)b.Zq * Npad;
     p.dq = static_cast<uint16_t*>(b.dq);
     p.dk = static_cast<uint16_t*>(b.dk);
     p.dv = static_cast<uint16_t*>(b.dv);
     p.status = b.status;
-    {
-        auto kern = dkdv_kernel<D>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        const int n_kt = (b.N + 127) / 128;
-        kern<<<(unsigned)(n_kt * Zk), kThreads, KvCfg<D>::kSmemBytes, stream>>>(mq64, mdo64, mk, mv, p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    {
-        auto kern = dq_kernel<D>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        const int n_qt = (b.N + 127) / 128;
-        kern<<<(unsigned)(n_qt * b.Zq), kThreads, DqCfg<D>::kSmemBytes, stream>>>(mq128, mdo128, mk, mv, p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    return p;
+}
+
+template <int D>
+cudaError_t pre_t(const BwdParams& b, cudaStream_t stream) {
+    const DevBwd p = dev_params(b);
+    const int64_t rows = (int64_t)b.Zq * p.Npad;
+    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(b.o), static_cast<const uint16_t*>(b.dout), b.lse, const_cast<float*>(p.dvec),
+        const_cast<float*>(p.lse2), b.Zq, b.N, p.Npad);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dkdv_t(const BwdParams& b, cudaStream_t stream) {
+    BwdMaps m;
+    if (!make_bwd_maps<D>(b, KvCfg<D>::kBQ, &m)) return cudaErrorInvalidValue;
+    auto kern = dkdv_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int n_kt = (b.N + 127) / 128;
+    kern<<<(unsigned)(n_kt * (b.Zq / b.g)), kThreads, KvCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v,
+                                                                                      dev_params(b));
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
+    BwdMaps m;
+    if (!make_bwd_maps<D>(b, DqCfg<D>::kBM, &m)) return cudaErrorInvalidValue;
+    auto kern = dq_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int n_qt = (b.N + 127) / 128;
+    kern<<<(unsigned)(n_qt * b.Zq), kThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_bf16(const BwdParams& b, cudaStream_t stream) {
-    if (b.d == 64) return launch_bwd_t<64>(b, stream);
-    if (b.d == 128) return launch_bwd_t<128>(b, stream);
-    return cudaErrorInvalidValue;
+cudaError_t launch_bwd_pre(const BwdParams& b, cudaStream_t stream) {
+    return b.d == 64 ? pre_t<64>(b, stream) : (b.d == 128 ? pre_t<128>(b, stream) : cudaErrorInvalidValue);
+}
+cudaError_t launch_bwd_dkdv(const BwdParams& b, cudaStream_t stream) {
+    return b.d == 64 ? dkdv_t<64>(b, stream) : (b.d == 128 ? dkdv_t<128>(b, stream) : cudaErrorInvalidValue);
+}
+cudaError_t launch_bwd_dq(const BwdParams& b, cudaStream_t stream) {
+    return b.d == 64 ? dq_t<64>(b, stream) : (b.d == 128 ? dq_t<128>(b, stream) : cudaErrorInvalidValue);
 }
 
 }  // namespace usp

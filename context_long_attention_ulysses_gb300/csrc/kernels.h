@@ -61,13 +61,17 @@ cudaError_t launch_attn_fwd_bf16(const FwdParams& p, cudaStream_t stream);
 struct BwdParams {
     const void *q, *k, *v, *o, *dout;
     const float* lse;
-    float* dvec;  // workspace: D_i = dO_i . O_i
+    float* dvec;  // workspace base: D_i = dO_i . O_i, then lse_i*log2(e), [Zq][Npad] each
     void *dq, *dk, *dv;
     int Zq, g, N, d, causal;
     float scale;
     int* status;
 };
-cudaError_t launch_attn_bwd_bf16(const BwdParams& p, cudaStream_t stream);
+// The three passes, in this order: D_i and lse_i*log2(e) into the workspace
+// (rows padded to 128), then dK/dV, then dQ.  p.dvec is the workspace base.
+cudaError_t launch_bwd_pre(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream);
 
 // ---- ring attention merge (ring.cu)
 cudaError_t launch_lse_merge(int64_t rows, int d, const float* o_a, const float* lse_a, const float* o_b,

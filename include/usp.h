@@ -75,8 +75,9 @@ typedef enum { USP_F32 = 0, USP_BF16 = 1 } usp_dtype;
  * K and V of shape B x Hkv x N x d, sequence-parallel degree P, causal flag
  * (is_causal), softmax scale (0 selects the default 1/sqrt(d)).
  * Requirements: B, N >= 0; Hq, Hkv, P >= 1; N % P == 0; Hq % Hkv == 0;
- * Hq % P == 0 and Hkv % P == 0 (every rank gets whole heads); d in {64, 128}
- * for attention. */
+ * B * Hq <= 65535; d in {64, 128} for attention.  Every entry point except
+ * the ring ones also needs Hq % P == 0 and Hkv % P == 0 (each rank gets whole
+ * heads after the all-to-all). */
 typedef struct {
     int B;
     int Hq;
@@ -117,8 +118,9 @@ usp_status usp_a2a_head2seq(const usp_problem* p, int Hx, const void* src, void*
 usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
                         float* lse, usp_stream stream);
 
-/* Bytes of workspace usp_attn_bwd needs: linear in N (one float32 per query
- * row), never quadratic.  Returns 0 for an invalid problem. */
+/* Bytes of workspace usp_attn_bwd needs: linear in N (two float32 per query
+ * row -- D_i and lse_i*log2(e) -- with rows padded to 128-row tiles), never
+ * quadratic.  Returns 0 for an invalid problem. */
 size_t usp_attn_bwd_workspace_size(const usp_problem* p);
 
 /* Attention backward on head-sharded buffers (the backward of the glossary
@@ -135,8 +137,9 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
                         const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                         size_t ws_bytes, usp_stream stream);
 
-/* Bytes of workspace usp_ring_attn_fwd needs (float32 running output and
- * LSE plus one float32 partial per query row): linear in N. */
+/* Bytes of workspace usp_ring_attn_fwd needs: a float32 running output and a
+ * float32 partial output (d values per query row) plus a float32 partial LSE
+ * per query row -- linear in N.  The running LSE lives in the caller's lse. */
 size_t usp_ring_workspace_size(const usp_problem* p);
 
 /* Ring attention forward on sequence-sharded buffers ("Context
@@ -161,6 +164,29 @@ usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k,
  * lse_a or lse_b (element-wise, in place).  d >= 1 and d % 4 == 0. */
 usp_status usp_ring_merge(int64_t rows, int d, const float* o_a, const float* lse_a, const float* o_b,
                           const float* lse_b, float* o, float* lse, usp_stream stream);
+
+/* ---- kernel tracing ----
+ * When enabled, every kernel the library launches is bracketed by two CUDA
+ * events recorded on the launch's stream (a few microseconds per launch).
+ * usp_trace_report() waits for the pending events and accumulates, per
+ * kernel name, the launch count and the summed event-to-event milliseconds.
+ * Tracing state is process-wide and not meant for concurrent threads. */
+typedef struct {
+    char name[32];    /* kernel name, e.g. "attn_fwd", "attn_bwd_dkdv", "a2a_seq2head" */
+    int64_t launches; /* launches since the last reset */
+    double total_ms;  /* summed durations */
+} usp_trace_entry;
+
+/* Turn tracing on (on != 0) or off.  Always USP_OK. */
+usp_status usp_trace_enable(int on);
+
+/* Drop pending events and accumulated totals.  Always USP_OK. */
+usp_status usp_trace_reset(void);
+
+/* Resolve pending events (this synchronises on them) and write up to
+ * max_entries totals into out (out may be NULL to query the count).
+ * Returns the number of distinct kernel names, or -1 if an event failed. */
+int usp_trace_report(usp_trace_entry* out, int max_entries);
 
 /* Synchronises `stream` and reads the device status word that bounded
  * device-side waits write: USP_OK, or USP_ERR_TIMEOUT (the word is then

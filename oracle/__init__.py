@@ -9,6 +9,9 @@ gcc and marshals numpy arrays to it.
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
 ``bench.py`` may import this package.  It shares no code with the CUDA path.
 
+``rows_blas`` restates the attention rows and gradients with numpy matrix
+products as the library step, for sampled rows of long sequences.
+
 Parity pins: every function here is checked by ``tests/test_oracle.py``
 against closed forms, library special cases, brute force and finite
 differences (see that file); no function is unpinned.

@@ -131,3 +131,11 @@ def test_workspaces_are_linear_in_sequence_length(lib):
         r2 = usp.usp_ring_workspace_size(_p(N=2 * N, Hq=32, Hkv=32, d=128, P=8))
         assert r2 == 2 * r1
     assert usp.usp_attn_bwd_workspace_size(_p(N=255)) == 0  # invalid problem
+
+
+def test_trace_report_without_launches(lib):
+    usp.usp_trace_reset()
+    usp.usp_trace_enable(True)
+    assert usp.usp_trace_report() == {}
+    usp.usp_trace_enable(False)
+    usp.usp_trace_reset()

@@ -349,3 +349,40 @@ def test_backward_row_subsets(orc):
     dvec_p[:, :, :3] = np.nan
     dk2, dv2 = orc.attn_bwd_kv_rows(q, k, v, dO, lse_p, dvec_p, rows=np.array([3, 20, 11]))
     assert np.array_equal(dk2, dk[:, :, [3, 20, 11]]) and np.array_equal(dv2, dv[:, :, [3, 20, 11]])
+
+
+# ------------------------------------------------ BLAS-backed row oracle (large sampled checks)
+@pytest.mark.parametrize("causal", [True, False])
+def test_blas_rows_match_c_oracle(orc, causal):
+    from oracle import rows_blas
+    B, Hq, Hkv, N, d = 2, 4, 2, 150, 16
+    q, k, v, dO = (_rand(s_, st, "bf16") for s_, st in (((B, Hq, N, d), 0), ((B, Hkv, N, d), 1),
+                                                         ((B, Hkv, N, d), 2), ((B, Hq, N, d), 3)))
+    rows = np.array([0, 1, 63, 64, 65, 100, 149], dtype=np.int64)
+    o, lse = orc.attn_rows(q, k, v, rows=rows, causal=causal)
+    o2, lse2 = rows_blas.attn_rows(q, k, v, rows, causal=causal)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
+    dq = orc.attn_bwd_q_rows(q, k, v, dO, rows=rows, causal=causal)
+    np.testing.assert_allclose(rows_blas.attn_bwd_q_rows(q, k, v, dO, rows, causal=causal), dq, rtol=0, atol=1e-11)
+    _, _, _, oa, lsea = orc.attn_bwd_full(q, k, v, dO, causal=causal)
+    dvec = np.einsum("bhnd,bhnd->bhn", orc.as_f64(dO), oa)
+    dk, dv = orc.attn_bwd_kv_rows(q, k, v, dO, lsea, dvec, rows=rows, causal=causal)
+    dk2, dv2 = rows_blas.attn_bwd_kv_rows(q, k, v, dO, lsea, dvec, rows, causal=causal)
+    np.testing.assert_allclose(dk2, dk, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv2, dv, rtol=0, atol=1e-11)
+
+
+def test_blas_rows_closed_forms():
+    from oracle import rows_blas
+    B, Hq, Hkv, N, d = 1, 4, 2, 40, 8
+    q, v = _rand((B, Hq, N, d), 0), _rand((B, Hkv, N, d), 2)
+    k = np.zeros((B, Hkv, N, d), np.float32)
+    rows = np.arange(N)
+    o, lse = rows_blas.attn_rows(q, k, v, rows, causal=True)
+    vf = np.repeat(v.astype(np.float64), 2, axis=1)
+    np.testing.assert_allclose(o, np.cumsum(vf, axis=2) / np.arange(1, N + 1)[None, None, :, None], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], np.log(np.arange(1, N + 1)), rtol=0, atol=1e-14)
+    vc = np.full_like(v, -1.25)
+    o, _ = rows_blas.attn_rows(q, _rand((B, Hkv, N, d), 1), vc, rows, causal=False)
+    np.testing.assert_allclose(o, -1.25, rtol=0, atol=1e-14)
