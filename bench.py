@@ -32,8 +32,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "causal SP-attention fwd+bwd TFLOP/s & % bf16 peak @128K; a2a remap GB/s"
-WORKLOAD = dict(B=1, Hq=32, Hkv=8, N=131072, d=128, P=8)
-WORKLOAD_NAME = "128K-token training step: Ulysses all-to-all + causal GQA attention fwd+bwd"
+WORKLOADS = {
+    "128k": (dict(B=1, Hq=32, Hkv=8, N=131072, d=128, P=8),
+             "128K-token training step: Ulysses all-to-all + causal GQA attention fwd+bwd"),
+    # smaller case of the same kernels (profiling captures): 32K tokens, 8192 per shard
+    "32k": (dict(B=1, Hq=32, Hkv=8, N=32768, d=128, P=4),
+            "32K-token GQA step: Ulysses all-to-all + causal GQA attention fwd+bwd"),
+}
+WORKLOAD, WORKLOAD_NAME = WORKLOADS["128k"]
 RING = dict(B=1, Hq=32, Hkv=32, N=524288, d=128, P=8)
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -115,6 +121,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ distributed
+def log(msg: str) -> None:
+    """Progress marker on stderr (the JSON line alone goes to stdout)."""
+    print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -248,6 +259,7 @@ def run_usp(args, world, rank, local):
     sh = stream.cuda_stream
 
     # ---- inputs: seeded logical tensors -> sequence-sharded -> pinned host -> HBM
+    log("generating inputs")
     q, k, v, do = oracle_inputs(w, seed=0)
 
     def pinned(x):
@@ -312,9 +324,11 @@ def run_usp(args, world, rank, local):
         barrier()
         return max_over_ranks(e0.elapsed_time(e1))
 
+    log("inputs resident; warm-up")
     for _ in range(args.warmup):
         step()
     barrier()
+    log("warm-up done; timed region")
     if usp.usp_device_status(sh) != 0:
         raise RuntimeError("device status reports a timed-out wait during warm-up")
 
@@ -331,6 +345,7 @@ def run_usp(args, world, rank, local):
     value = world * flops_step / (ms * 1e-3) / 1e12
 
     # ---- end to end: host buffers in, host buffers out, every step
+    log(f"timed region done ({ms:.1f} ms/step); end-to-end leg")
     e2e_step()
     e2e_ms = timed(e2e_step, args.steps) / args.steps
     h2d = sum(t.numel() * t.element_size() for t in host_in)
@@ -372,6 +387,7 @@ def run_usp(args, world, rank, local):
 
     ring = None
     if args.ring and rank == 0:
+        log("ring leg")
         ring = bench_ring(usp, torch, dev, peaks)
 
     line = {
@@ -396,6 +412,7 @@ def run_usp(args, world, rank, local):
     if ring is not None:
         line["ring"] = ring
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        log("cpu baseline (oracle)")
         line["cpu_baseline"] = cpu_baseline(w, cpu_inputs, rows_per_head=args.cpu_rows)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -407,14 +424,19 @@ def run_usp(args, world, rank, local):
 
 def bench_ring(usp, torch, dev, peaks):
     """Ring attention forward on the 512K-token workload (one timed call)."""
+    import numpy as np
+    import synth
     w = RING
     p = usp.Problem(**w, causal=True)
-    g = torch.Generator(device=dev)
-    g.manual_seed(0)
-    shape_q = p.seq_shape(w["Hq"])
-    q = torch.randn(shape_q, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    k = torch.randn(p.seq_shape(w["Hkv"]), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn(p.seq_shape(w["Hkv"]), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    def upload(shape, stream_id):
+        # seeded N(0,1) bf16, generated directly in the sequence-sharded layout (iid samples)
+        x = synth.normal(shape, seed=0, stream=stream_id, dtype="bf16")
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q = upload(p.seq_shape(w["Hq"]), synth.STREAM_Q)
+    k = upload(p.seq_shape(w["Hkv"]), synth.STREAM_K)
+    v = upload(p.seq_shape(w["Hkv"]), synth.STREAM_V)
     o = torch.empty_like(q)
     lse = torch.empty(p.lse_seq_shape(), dtype=torch.float32, device=dev)
     ws = torch.empty(usp.usp_ring_workspace_size(p), dtype=torch.uint8, device=dev)
@@ -438,7 +460,7 @@ def bench_ring(usp, torch, dev, peaks):
     return {"workload": "512K-token ring attention forward, B=1, H=32, d=128, P=8 (shards of 65536)",
             "ms": ms, "TFLOPs": f / (ms * 1e-3) / 1e12, "frac_sustained": f / (ms * 1e-3) / 1e12 / peaks["bf16_sus"],
             "kernels_ms": {k_: v_[1] for k_, v_ in trace.items()}, "status_ok": ok,
-            "data": "torch device RNG N(0,1), seed 0"}
+            "data": "seeded Philox N(0,1) bf16 (seed 0, streams Q/K/V), sequence-sharded"}
 
 
 def main():
@@ -450,7 +472,10 @@ def main():
     ap.add_argument("--no-ring", dest="ring", action="store_false", help="skip the 512K ring measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows per head for cpu_baseline")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="128k")
     args = ap.parse_args()
+    global WORKLOAD, WORKLOAD_NAME
+    WORKLOAD, WORKLOAD_NAME = WORKLOADS[args.workload]
     args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
     world, rank, local = dist_setup()
     if args.impl == "reference":
