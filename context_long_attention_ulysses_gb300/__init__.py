@@ -19,14 +19,15 @@ from dataclasses import dataclass
 
 import torch
 
-from ._lib import (SYMBOLS, USP_BF16, USP_F32, USP_OK, UspError, UspProblem, UspTraceEntry, check,  # noqa: F401
-                   load)
+from ._lib import (NOALLOC_SCRATCH_BYTES, SYMBOLS, USP_BF16, USP_F32, USP_OK, UspError, UspProblem,  # noqa: F401
+                   UspTraceEntry, check, load)
 
 __all__ = [
     "Problem", "UspError", "SYMBOLS",
     "usp_a2a_seq2head", "usp_a2a_head2seq", "usp_attn_fwd", "usp_attn_bwd_workspace_size", "usp_attn_bwd",
     "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
-    "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "ulysses_attention_fwd", "ulysses_attention_bwd", "ring_attention_fwd", "library_path",
+    "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "usp_attn_bwd_noalloc",
+    "NOALLOC_SCRATCH_BYTES", "ulysses_attention_fwd", "ulysses_attention_bwd", "ring_attention_fwd", "library_path",
 ]
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -131,6 +132,18 @@ def usp_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream
     check("usp_attn_bwd", load().usp_attn_bwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
                                               _stream(stream)))
+
+
+def usp_attn_bwd_noalloc(p, q, k, v, o, lse, dout, dq, dk, dv, stream=None) -> None:
+    """usp_attn_bwd with the library's built-in scratch instead of a workspace.
+
+    For callers that cannot allocate device memory.  Problems needing more
+    than NOALLOC_SCRATCH_BYTES of workspace raise UspError (USP_ERR_WORKSPACE);
+    calls that may overlap on the GPU share the scratch and must be serialised.
+    """
+    check("usp_attn_bwd_noalloc", load().usp_attn_bwd_noalloc(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                              _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                                              _stream(stream)))
 
 
 def usp_ring_workspace_size(p) -> int:

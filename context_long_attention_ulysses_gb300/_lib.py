@@ -19,6 +19,8 @@ USP_ERR_WORKSPACE = 4
 USP_ERR_CUDA = 5
 USP_ERR_TIMEOUT = 6
 
+NOALLOC_SCRATCH_BYTES = 64 << 20  # USP_NOALLOC_SCRATCH_BYTES
+
 USP_F32 = 0
 USP_BF16 = 1
 
@@ -26,7 +28,7 @@ USP_BF16 = 1
 SYMBOLS = (
     "usp_a2a_seq2head", "usp_a2a_head2seq", "usp_attn_fwd", "usp_attn_bwd_workspace_size", "usp_attn_bwd",
     "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
-    "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report",
+    "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "usp_attn_bwd_noalloc",
 )
 
 
@@ -83,6 +85,7 @@ def load() -> ctypes.CDLL:
             "usp_trace_enable": (ci, [ci]),
             "usp_trace_reset": (ci, []),
             "usp_trace_report": (ci, [ctypes.POINTER(UspTraceEntry), ci]),
+            "usp_attn_bwd_noalloc": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

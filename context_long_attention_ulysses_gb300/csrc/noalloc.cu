@@ -1,0 +1,61 @@
+// Attention backward for callers that cannot allocate device memory.
+//
+// usp_attn_bwd needs a caller-provided workspace (two float32 values per
+// query row).  Some callers cannot obtain one: code running inside a
+// framework that owns every device allocation and forbids raw cudaMalloc,
+// plugins loaded into a host process that has no allocator to hand them, or
+// code that must not touch the allocator at all once set up.  This file gives
+// them usp_attn_bwd_noalloc, which uses a fixed scratch array compiled into
+// the library instead.
+//
+// The scratch is a file-scope __device__ array of USP_NOALLOC_SCRATCH_BYTES.
+// Every GPU that loads the library holds it until the process exits.  Host
+// code cannot use the array's name as a device address (it names a host-side
+// stand-in), so the address is looked up with cudaGetSymbolAddress once per
+// device, with that device current, on the first call made on it.
+#include <mutex>
+
+#include "../../include/usp.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = USP_NOALLOC_SCRATCH_BYTES;
+static_assert(kScratchBytes % 256 == 0, "scratch size must keep 256-byte alignment");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on first use).
+usp_status scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return USP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return USP_ERR_CUDA;
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return USP_OK;
+}
+
+}  // namespace
+
+extern "C" usp_status usp_attn_bwd_noalloc(const usp_problem* p, const void* q, const void* k, const void* v,
+                                           const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                                           void* dv, usp_stream stream) {
+    // Size checks first: a problem the scratch cannot hold is rejected before any CUDA call.
+    const size_t need = usp_attn_bwd_workspace_size(p);
+    if (need == 0)  // an invalid problem (rejected) or an empty one (nothing to do): no scratch involved
+        return usp_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, nullptr, 0, stream);
+    if (need > kScratchBytes) return USP_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    usp_status st = scratch_address(&scratch);
+    if (st != USP_OK) return st;
+    // The backward's first pass rewrites every scratch entry the later passes
+    // read, so the previous call's contents never matter.
+    return usp_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, scratch, kScratchBytes, stream);
+}

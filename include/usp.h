@@ -137,6 +137,34 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
                         const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                         size_t ws_bytes, usp_stream stream);
 
+/* Size of the scratch array built into the library for
+ * usp_attn_bwd_noalloc: 64 MiB, enough for B*Hq*roundup(N,128) <= 8 Mi query
+ * rows (e.g. 32 heads of 262 144 tokens). */
+#define USP_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* usp_attn_bwd for callers that cannot allocate device memory -- code inside
+ * a framework that owns every device allocation, plugins handed no
+ * allocator, or code that must not call the allocator once running.  The
+ * pages have no counterpart to this entry point; it exists for such callers.
+ * Same arguments, layouts and results as usp_attn_bwd, minus the workspace:
+ * the workspace is a file-scope device array of USP_NOALLOC_SCRATCH_BYTES
+ * inside the library, held on every GPU that loads it until the process
+ * exits.  Nothing is allocated or freed by the call.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture.
+ *  - Size limit: problems needing more than USP_NOALLOC_SCRATCH_BYTES
+ *    (usp_attn_bwd_workspace_size) return USP_ERR_WORKSPACE with nothing
+ *    enqueued.
+ *  - Sharing: every call on a device uses the same array, and the array keeps
+ *    the last call's contents (each call rewrites every entry it reads before
+ *    reading it).  Calls that can overlap on the GPU -- on different streams,
+ *    or from different host threads -- race on the array and must be
+ *    serialised by the caller. */
+usp_status usp_attn_bwd_noalloc(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                usp_stream stream);
+
 /* Bytes of workspace usp_ring_attn_fwd needs: a float32 running output and a
  * float32 partial output (d values per query row) plus a float32 partial LSE
  * per query row -- linear in N.  The running LSE lives in the caller's lse. */
