@@ -107,7 +107,7 @@ struct KvCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kKVBytes = kChunks * kBK * 128;
     static constexpr int kQBytes = kChunks * kBQ * 128;
-    static constexpr int kStages = 3;
+    static constexpr int kStages = 4;
     static constexpr int kVecBytes = 2 * kBQ * 4;  // lse2 then dvec of one query tile
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kKVBytes;
@@ -200,25 +200,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (n_it > 0 && warp == kMmaWarp && lane == 0) {
         constexpr uint32_t kIdS = idesc_bf16(C::kBK, C::kBQ, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
         constexpr uint32_t kIdG = idesc_bf16(C::kBK, D, 0, 1);       // dV += P^T dO, dK += dS^T Q
-        const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV;
+        // descriptors built once; each k-step adds its offset (address field, 16-byte units)
+        const uint64_t dk0 = sdesc_sw128(sbase + C::kOffK, 16, 1024), dv0 = sdesc_sw128(sbase + C::kOffV, 16, 1024);
         auto issue_s = [&](int it) -> bool {
             const int s = it % C::kStages;
             if (!mbar_wait(BAR(kQFull + s), (it / C::kStages) & 1, abort_p, 22, p.status)) return false;
             tc_fence_after();
-            const uint32_t sQ = sbase + C::kOffQ + s * C::kQBytes, sDO = sbase + C::kOffDO + s * C::kQBytes;
+            const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ + s * C::kQBytes, 16, 1024);
+            const uint64_t ddo0 = sdesc_sw128(sbase + C::kOffDO + s * C::kQBytes, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t a_off = (kk / 4) * (C::kBK * 128) + (kk % 4) * 32;
-                const uint32_t b_off = (kk / 4) * (C::kBQ * 128) + (kk % 4) * 32;
-                mma_ss(tmem + C::kColS, sdesc_sw128(sK + a_off, 16, 1024), sdesc_sw128(sQ + b_off, 16, 1024), kIdS,
-                       kk > 0);
+                const uint32_t a_off = ((kk / 4) * (C::kBK * 128) + (kk % 4) * 32) >> 4;
+                const uint32_t b_off = ((kk / 4) * (C::kBQ * 128) + (kk % 4) * 32) >> 4;
+                mma_ss(tmem + C::kColS, dk0 + a_off, dq0 + b_off, kIdS, kk > 0);
             }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t a_off = (kk / 4) * (C::kBK * 128) + (kk % 4) * 32;
-                const uint32_t b_off = (kk / 4) * (C::kBQ * 128) + (kk % 4) * 32;
-                mma_ss(tmem + C::kColDP, sdesc_sw128(sV + a_off, 16, 1024), sdesc_sw128(sDO + b_off, 16, 1024), kIdS,
-                       kk > 0);
+                const uint32_t a_off = ((kk / 4) * (C::kBK * 128) + (kk % 4) * 32) >> 4;
+                const uint32_t b_off = ((kk / 4) * (C::kBQ * 128) + (kk % 4) * 32) >> 4;
+                mma_ss(tmem + C::kColDP, dv0 + a_off, ddo0 + b_off, kIdS, kk > 0);
             }
             mma_commit(BAR(kSFull));
             return true;
@@ -233,17 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!mbar_wait(BAR(kPReady + (it & 1)), (it >> 1) & 1, abort_p, 25, p.status)) break;
             tc_fence_after();
-            const uint32_t sQ = sbase + C::kOffQ + s * C::kQBytes, sDO = sbase + C::kOffDO + s * C::kQBytes;
+            const uint64_t bdo = sdesc_sw128(sbase + C::kOffDO + s * C::kQBytes, C::kBQ * 128, 1024);
+            const uint64_t bq = sdesc_sw128(sbase + C::kOffQ + s * C::kQBytes, C::kBQ * 128, 1024);
             const uint32_t pt = tmem + ((it & 1) ? C::kColPt1 : C::kColPt0);
             const uint32_t dst = tmem + ((it & 1) ? C::kColDSt1 : C::kColDSt0);
 #pragma unroll
             for (int kk = 0; kk < C::kBQ / 16; ++kk)
-                mma_ts(tmem + C::kColDV, pt + kk * 8, sdesc_sw128(sDO + kk * 2048, C::kBQ * 128, 1024), kIdG,
-                       (it > 0 || kk > 0) ? 1u : 0u);
+                mma_ts(tmem + C::kColDV, pt + kk * 8, bdo + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < C::kBQ / 16; ++kk)
-                mma_ts(tmem + C::kColDK, dst + kk * 8, sdesc_sw128(sQ + kk * 2048, C::kBQ * 128, 1024), kIdG,
-                       (it > 0 || kk > 0) ? 1u : 0u);
+                mma_ts(tmem + C::kColDK, dst + kk * 8, bq + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
             mma_commit(BAR(kQEmpty + s));
             if (it + 1 == n_it) mma_commit(BAR(kOReady));
         }
@@ -350,13 +349,15 @@ struct DqCfg {
     static constexpr int kBN = 128;  // keys per step
     static constexpr int kChunks = D / 64;
     static constexpr int kTile = kChunks * 128 * 128;
-    static constexpr int kStages = D == 64 ? 3 : 2;
+    // K is held until dQ's product, V only until dP's: separate rings, K deeper
+    static constexpr int kKStages = D == 64 ? 4 : 3;
+    static constexpr int kVStages = D == 64 ? 3 : 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffDO = kTile;
     static constexpr int kOffK = 2 * kTile;
-    static constexpr int kOffV = kOffK + kStages * kTile;
-    static constexpr int kOffBar = kOffV + kStages * kTile;
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1;
+    static constexpr int kOffV = kOffK + kKStages * kTile;
+    static constexpr int kOffBar = kOffV + kVStages * kTile;
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDS0 = 256, kColDS1 = 320, kColDQ = 384;
 };
@@ -373,7 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int abort_flag;
     const uint32_t bar0 = sbase + C::kOffBar;
     auto BAR = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
-    const int kQFull = 0, kKvFull = 1, kKvEmpty = 1 + C::kStages, kSFull = 1 + 2 * C::kStages, kSFree = kSFull + 1,
+    const int kQFull = 0, kKFull = 1, kKEmpty = kKFull + C::kKStages, kVFull = kKEmpty + C::kKStages,
+              kVEmpty = kVFull + C::kVStages, kSFull = kVEmpty + C::kVStages, kSFree = kSFull + 1,
               kDsReady = kSFree + 1, kOReady = kDsReady + 2;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -387,9 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(BAR(kQFull), 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(BAR(kKvFull + s), 1);
-            mbar_init(BAR(kKvEmpty + s), 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(BAR(kKFull + s), 1);
+            mbar_init(BAR(kKEmpty + s), 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(BAR(kVFull + s), 1);
+            mbar_init(BAR(kVEmpty + s), 1);
         }
         mbar_init(BAR(kSFull), 1);
         mbar_init(BAR(kSFree), kSoftmaxWarps * 32);
@@ -419,57 +425,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(sbase + C::kOffDO + c * 16384, &tm_do, c * 64, zq, qt * C::kBM, 0, BAR(kQFull));
         }
         for (int j = 0; j < n_it; ++j) {
-            const int s = j % C::kStages;
-            if (j >= C::kStages && !mbar_wait(BAR(kKvEmpty + s), ((j / C::kStages) - 1) & 1, abort_p, 31, p.status))
+            const int ks = j % C::kKStages, vs = j % C::kVStages;
+            if (j >= C::kKStages &&
+                !mbar_wait(BAR(kKEmpty + ks), ((j / C::kKStages) - 1) & 1, abort_p, 31, p.status))
                 break;
-            mbar_arrive_expect_tx(BAR(kKvFull + s), 2 * C::kTile);
-            for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_4d(sbase + C::kOffK + s * C::kTile + c * 16384, &tm_k, c * 64, zk, j * C::kBN, 0,
-                            BAR(kKvFull + s));
-                tma_load_4d(sbase + C::kOffV + s * C::kTile + c * 16384, &tm_v, c * 64, zk, j * C::kBN, 0,
-                            BAR(kKvFull + s));
-            }
+            mbar_arrive_expect_tx(BAR(kKFull + ks), C::kTile);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(sbase + C::kOffK + ks * C::kTile + c * 16384, &tm_k, c * 64, zk, j * C::kBN, 0,
+                            BAR(kKFull + ks));
+            if (j >= C::kVStages &&
+                !mbar_wait(BAR(kVEmpty + vs), ((j / C::kVStages) - 1) & 1, abort_p, 38, p.status))
+                break;
+            mbar_arrive_expect_tx(BAR(kVFull + vs), C::kTile);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(sbase + C::kOffV + vs * C::kTile + c * 16384, &tm_v, c * 64, zk, j * C::kBN, 0,
+                            BAR(kVFull + vs));
         }
     } else if (n_it > 0 && warp == kMmaWarp && lane == 0) {
         constexpr uint32_t kIdS = idesc_bf16(C::kBM, C::kBN, 0, 0);  // S = Q K^T, dP = dO V^T
         constexpr uint32_t kIdG = idesc_bf16(C::kBM, D, 0, 1);       // dQ += dS K, K MN-major
-        const uint32_t sQ = sbase + C::kOffQ, sDO = sbase + C::kOffDO;
+        // descriptors built once; each k-step adds its offset (address field, 16-byte units)
+        const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ, 16, 1024), ddo0 = sdesc_sw128(sbase + C::kOffDO, 16, 1024);
         auto issue_s = [&](int j) -> bool {
-            const int s = j % C::kStages;
-            if (!mbar_wait(BAR(kKvFull + s), (j / C::kStages) & 1, abort_p, 32, p.status)) return false;
+            const int ks = j % C::kKStages, vs = j % C::kVStages;
+            if (!mbar_wait(BAR(kKFull + ks), (j / C::kKStages) & 1, abort_p, 32, p.status)) return false;
+            if (!mbar_wait(BAR(kVFull + vs), (j / C::kVStages) & 1, abort_p, 39, p.status)) return false;
             tc_fence_after();
-            const uint32_t sK = sbase + C::kOffK + s * C::kTile, sV = sbase + C::kOffV + s * C::kTile;
+            const uint64_t dk0 = sdesc_sw128(sbase + C::kOffK + ks * C::kTile, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sbase + C::kOffV + vs * C::kTile, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                mma_ss(tmem + C::kColS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdS, kk > 0);
+                const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                mma_ss(tmem + C::kColS, dq0 + off, dk0 + off, kIdS, kk > 0);
             }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                mma_ss(tmem + C::kColDP, sdesc_sw128(sDO + off, 16, 1024), sdesc_sw128(sV + off, 16, 1024), kIdS,
-                       kk > 0);
+                const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                mma_ss(tmem + C::kColDP, ddo0 + off, dv0 + off, kIdS, kk > 0);
             }
             mma_commit(BAR(kSFull));
+            mma_commit(BAR(kVEmpty + vs));  // V_j is no longer needed once dP_j is done
             return true;
         };
         bool ok = mbar_wait(BAR(kQFull), 0, abort_p, 33, p.status);
         ok = ok && issue_s(0);
         for (int j = 0; ok && j < n_it; ++j) {
-            const int s = j % C::kStages;
+            const int ks = j % C::kKStages;
             if (j + 1 < n_it) {
                 if (!mbar_wait(BAR(kSFree), j & 1, abort_p, 34, p.status)) break;
                 if (!issue_s(j + 1)) break;
             }
             if (!mbar_wait(BAR(kDsReady + (j & 1)), (j >> 1) & 1, abort_p, 35, p.status)) break;
             tc_fence_after();
-            const uint32_t sK = sbase + C::kOffK + s * C::kTile;
+            const uint64_t bk = sdesc_sw128(sbase + C::kOffK + ks * C::kTile, 16384, 1024);
             const uint32_t ds = tmem + ((j & 1) ? C::kColDS1 : C::kColDS0);
 #pragma unroll
             for (int kk = 0; kk < C::kBN / 16; ++kk)
-                mma_ts(tmem + C::kColDQ, ds + kk * 8, sdesc_sw128(sK + kk * 2048, 16384, 1024), kIdG,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(BAR(kKvEmpty + s));
+                mma_ts(tmem + C::kColDQ, ds + kk * 8, bk + (kk * 2048 >> 4), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(BAR(kKEmpty + ks));
             if (j + 1 == n_it) mma_commit(BAR(kOReady));
         }
     } else if (warp < kSoftmaxWarps) {

@@ -43,8 +43,9 @@ template <int D>
 struct FwdCfg {
     static constexpr int kChunks = D / 64;                 // 64-column (128-byte) swizzle atoms per row
     static constexpr int kTileBytes = kChunks * 128 * 128; // one 128-row bf16 tile
-    static constexpr int kKStages = D == 64 ? 3 : 2;
-    static constexpr int kVStages = D == 64 ? 3 : 2;
+    // three (d=128) or four (d=64) tiles in flight per ring hide the L2->SMEM latency
+    static constexpr int kKStages = D == 64 ? 4 : 3;
+    static constexpr int kVStages = D == 64 ? 4 : 3;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
@@ -183,17 +184,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- MMA issuer
         constexpr uint32_t kIdS = idesc_bf16(kBM, kBN, 0, 0);  // S = Q K^T, both K-major
         constexpr uint32_t kIdO = idesc_bf16(kBM, D, 0, 1);    // O += P V, V MN-major
-        const uint32_t sQ = sbase + C::kOffQ;
+        const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ, 16, 1024);  // built once; k-steps add offsets
         auto issue_qk = [&](int j) -> bool {
             const int ks = j % C::kKStages;
             if (!mbar_wait(BAR(kKFull + ks), (j / C::kKStages) & 1, abort_p, 3, p.status)) return false;
             tc_fence_after();
-            const uint32_t sK = sbase + C::kOffK + ks * C::kTileBytes;
+            const uint64_t dk0 = sdesc_sw128(sbase + C::kOffK + ks * C::kTileBytes, 16, 1024);
             const uint32_t dcol = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                mma_ss(dcol, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdS, kk > 0);
+                const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;  // descriptor address units
+                mma_ss(dcol, dq0 + off, dk0 + off, kIdS, kk > 0);
             }
             mma_commit(BAR(kSFull + (j & 1)));
             mma_commit(BAR(kKEmpty + ks));
@@ -207,12 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(BAR(kPReady + (j & 1)), (j >> 1) & 1, abort_p, 5, p.status)) break;
             if (!mbar_wait(BAR(kVFull + vs), (j / C::kVStages) & 1, abort_p, 6, p.status)) break;
             tc_fence_after();
-            const uint32_t sV = sbase + C::kOffV + vs * C::kTileBytes;
+            const uint64_t dv0 = sdesc_sw128(sbase + C::kOffV + vs * C::kTileBytes, 16384, 1024);
             const uint32_t pcol = tmem + ((j & 1) ? C::kColP1 : C::kColP0);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_ts(tmem + C::kColO, pcol + kk * 8, sdesc_sw128(sV + kk * 2048, 16384, 1024), kIdO,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+                mma_ts(tmem + C::kColO, pcol + kk * 8, dv0 + (kk * 2048 >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(BAR(kVEmpty + vs));
             mma_commit(BAR(kPvDone));
             if (j + 2 < w.n_tiles) ok = issue_qk(j + 2);
@@ -255,16 +255,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN; ++c)
                     if (c > climit) s[c] = -INFINITY;
             }
-            float mx = s[0];
+            // row max as eight independent chains (a single chain would be 128 dependent ops)
+            float m8[8];
 #pragma unroll
-            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+            for (int c = 0; c < 8; ++c) m8[c] = s[c];
+#pragma unroll
+            for (int c = 8; c < kBN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             mx *= p.scale_log2;
             const float m_new = fmaxf(m_run, mx);
             const bool rescale = m_new > m_run + kRescaleThreshold;
             const float m_use = rescale ? m_new : m_run;
             const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
             const float msub = m_use == -INFINITY ? 0.f : m_use;
-            float sum = 0.f;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: independent chains
             const uint32_t pcol = lane_base + ((j & 1) ? C::kColP1 : C::kColP0);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -273,12 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 16; ++c) {
                     const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * c], p.scale_log2, -msub));
                     const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * c + 1], p.scale_log2, -msub));
-                    sum += p0 + p1;
+                    sum4[c & 3] += p0 + p1;
                     pk[c] = pack_bf16(p0, p1);
                 }
                 tmem_st16(pcol + h * 16, pk);
             }
-            l_run = l_run * alpha + sum;
+            l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
             if (rescale && j > 0) {
                 // O holds PV of tiles < j: wait for the last of them, then scale in place
                 if (!mbar_wait(BAR(kPvDone), (j - 1) & 1, abort_p, 8, p.status)) { ok = false; break; }

@@ -183,6 +183,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), version 1 at bits 46-47, layout type at
 // bits 61-63 (2 = 128-byte swizzle).  Atoms must sit on 1024-byte boundaries.
+// The start address is the low 14-bit field: a descriptor for base + off is
+// the base descriptor plus off >> 4 (shared addresses stay below 256 KB, so
+// the field never carries).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
