@@ -9,17 +9,22 @@
 // ("So funktioniert Kontextparallelitaet" on the same page).
 //
 // One CTA owns a 128-row query tile and walks the visible 128-key tiles:
-//   warp 4      TMA producer: Q once, then K_j and V_j into 2-3 stage rings
+//   warp 4      TMA producer: K_j and V_j into 3-4 stage rings
 //   warp 5      TMEM owner + single-thread tcgen05.mma issuer:
-//                 S_j = Q K_j^T  (both operands K-major in shared memory)
+//                 S_j = Q K_j^T  (Q from TMEM as bf16, K_j K-major in shared memory)
 //                 O  += P_j V_j  (P_j from TMEM as bf16, V_j MN-major)
 //   warps 0-3   softmax: thread = query row = TMEM lane; online softmax in
 //               the log2 domain with lazy rescaling of O (only when the
 //               running max grows by more than 2^8), P written back to TMEM
 //               as bf16, final normalisation, O and LSE stores.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P0, P1 (64 each).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P (64), Q (D/2).
 // S is double-buffered so QK^T of tile j+2 and PV of tile j run on the tensor
-// core while the softmax works on tile j+1.
+// core while the softmax works on tile j+1.  Q sits in TMEM (staged once by
+// the softmax threads from global memory) so that the tensor core reads only
+// K and V from shared memory: per tile 32 KB K + 32 KB V of MMA reads plus
+// 64 KB of TMA writes, which shared-memory bandwidth (128 B/clk) serves in
+// the 1024 cycles the two 128x128x128 products take.  P is single-buffered:
+// the softmax of tile j writes it only after PV of tile j-1 has completed.
 #include <cmath>
 
 #include "kernels.h"
@@ -43,20 +48,22 @@ template <int D>
 struct FwdCfg {
     static constexpr int kChunks = D / 64;                 // 64-column (128-byte) swizzle atoms per row
     static constexpr int kTileBytes = kChunks * 128 * 128; // one 128-row bf16 tile
-    // three (d=128) or four (d=64) tiles in flight per ring hide the L2->SMEM latency
-    static constexpr int kKStages = D == 64 ? 4 : 3;
+    // 3-4 tiles in flight per ring hide the L2->SMEM latency (Q lives in TMEM, not here)
+    static constexpr int kKStages = 4;
     static constexpr int kVStages = D == 64 ? 4 : 3;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
     static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot, + alignment slack
-    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 256 + D, kColP1 = 256 + D + 64;
+    // TMEM: S double-buffered, O, P (bf16, single), Q (bf16, the A operand of Q K^T)
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 256 + D, kColQ = 256 + D + 64;
     static constexpr uint32_t kTmemCols = 512;
 };
 
 struct DevFwd {
+    const uint16_t* q;                       // bf16 Q, addressed like Tensor4
+    int64_t q_s_head, q_s_tok, q_s_outer;    // elements
     int d, g, n_heads, n_outer, q_len, kv_len;
     int ring_i0, ring_t, ring_p, bsz, np;
     int causal;
@@ -109,8 +116,7 @@ __device__ __forceinline__ WorkItem decode_item(const DevFwd& p) {
 
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const DevFwd p) {
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevFwd p) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(BAR(kQFull), 1);
+        mbar_init(BAR(kQFull), kSoftmaxWarps * 32);  // the softmax threads stage Q into TMEM
         for (int s = 0; s < C::kKStages; ++s) { mbar_init(BAR(kKFull + s), 1); mbar_init(BAR(kKEmpty + s), 1); }
         for (int s = 0; s < C::kVStages; ++s) { mbar_init(BAR(kVFull + s), 1); mbar_init(BAR(kVEmpty + s), 1); }
         for (int s = 0; s < 2; ++s) {
@@ -159,12 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (w.n_tiles > 0 && warp == kProducerWarp && lane == 0) {
         // ---------------------------------------------------------------- TMA producer
-        tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(BAR(kQFull), C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sbase + C::kOffQ + c * 16384, &tm_q, c * 64, w.head, w.r0, w.q_outer, BAR(kQFull));
         for (int j = 0; j < w.n_tiles; ++j) {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
             if (j >= C::kKStages && !mbar_wait(BAR(kKEmpty + ks), ((j / C::kKStages) - 1) & 1, abort_p, 1, p.status))
@@ -184,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- MMA issuer
         constexpr uint32_t kIdS = idesc_bf16(kBM, kBN, 0, 0);  // S = Q K^T, both K-major
         constexpr uint32_t kIdO = idesc_bf16(kBM, D, 0, 1);    // O += P V, V MN-major
-        const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ, 16, 1024);  // built once; k-steps add offsets
         auto issue_qk = [&](int j) -> bool {
             const int ks = j % C::kKStages;
             if (!mbar_wait(BAR(kKFull + ks), (j / C::kKStages) & 1, abort_p, 3, p.status)) return false;
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;  // descriptor address units
-                mma_ss(dcol, dq0 + off, dk0 + off, kIdS, kk > 0);
+                mma_ts(dcol, tmem + C::kColQ + kk * 8, dk0 + off, kIdS, kk > 0);  // A = Q from TMEM
             }
             mma_commit(BAR(kSFull + (j & 1)));
             mma_commit(BAR(kKEmpty + ks));
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(BAR(kVFull + vs), (j / C::kVStages) & 1, abort_p, 6, p.status)) break;
             tc_fence_after();
             const uint64_t dv0 = sdesc_sw128(sbase + C::kOffV + vs * C::kTileBytes, 16384, 1024);
-            const uint32_t pcol = tmem + ((j & 1) ? C::kColP1 : C::kColP0);
+            const uint32_t pcol = tmem + C::kColP;
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
                 mma_ts(tmem + C::kColO, pcol + kk * 8, dv0 + (kk * 2048 >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
@@ -226,6 +227,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_run = -INFINITY;  // running max of scale*log2(e)*S over the row (log2 units)
         float l_run = 0.f;        // running sum of 2^(scaled S - m_run)
         bool ok = true;
+        if (w.n_tiles > 0) {
+            // Q row -> TMEM (A operand of Q K^T): bf16 pairs packed per 32-bit column, zeros past q_len
+            const int tok = w.r0 + row;
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + (int64_t)w.head * p.q_s_head +
+                                                              (int64_t)tok * p.q_s_tok +
+                                                              (int64_t)w.q_outer * p.q_s_outer);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t qr[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 v = tok < p.q_len ? __ldg(src + c * 8 + e) : make_uint4(0u, 0u, 0u, 0u);
+                    qr[4 * e] = v.x;
+                    qr[4 * e + 1] = v.y;
+                    qr[4 * e + 2] = v.z;
+                    qr[4 * e + 3] = v.w;
+                }
+                tmem_st32(lane_base + C::kColQ + c * 32, qr);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(kQFull));
+        }
         for (int j = 0; j < w.n_tiles; ++j) {
             if (!mbar_wait(BAR(kSFull + (j & 1)), (j >> 1) & 1, abort_p, 7, p.status)) { ok = false; break; }
             tc_fence_after();
@@ -270,24 +294,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
             const float msub = m_use == -INFINITY ? 0.f : m_use;
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: independent chains
-            const uint32_t pcol = lane_base + ((j & 1) ? C::kColP1 : C::kColP0);
+            uint32_t pk0[32], pk1[32];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * c], p.scale_log2, -msub));
-                    const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * c + 1], p.scale_log2, -msub));
-                    sum4[c & 3] += p0 + p1;
-                    pk[c] = pack_bf16(p0, p1);
-                }
-                tmem_st16(pcol + h * 16, pk);
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, -msub));
+                const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, -msub));
+                const float p2 = ex2_approx(fmaf(s[64 + 2 * c], p.scale_log2, -msub));
+                const float p3 = ex2_approx(fmaf(s[64 + 2 * c + 1], p.scale_log2, -msub));
+                sum4[c & 3] += (p0 + p1) + (p2 + p3);
+                pk0[c] = pack_bf16(p0, p1);
+                pk1[c] = pack_bf16(p2, p3);
             }
             l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-            if (rescale && j > 0) {
-                // O holds PV of tiles < j: wait for the last of them, then scale in place
+            if (j > 0) {
+                // P and O are read by PV of tile j-1: wait until it has completed (QK of tile j was
+                // issued after PV of tile j-2, so at most PV j-1 is outstanding: the parity test is exact)
                 if (!mbar_wait(BAR(kPvDone), (j - 1) & 1, abort_p, 8, p.status)) { ok = false; break; }
                 tc_fence_after();
+            }
+            tmem_st32(lane_base + C::kColP, pk0);
+            tmem_st32(lane_base + C::kColP + 32, pk1);
+            if (rescale && j > 0) {
+                // O holds PV of tiles < j (all complete): scale in place
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -361,10 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool OUT_F32>
 cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
     using C = FwdCfg<D>;
-    CUtensorMap tq, tk, tv;
-    if (!make_tmap_bf16(&tq, f.q, D, kBM) || !make_tmap_bf16(&tk, f.k, D, kBN) || !make_tmap_bf16(&tv, f.v, D, kBN))
-        return cudaErrorInvalidValue;
+    CUtensorMap tk, tv;
+    if (!make_tmap_bf16(&tk, f.k, D, kBN) || !make_tmap_bf16(&tv, f.v, D, kBN)) return cudaErrorInvalidValue;
     DevFwd p;
+    p.q = static_cast<const uint16_t*>(f.q.ptr);
+    p.q_s_head = f.q.s_head;
+    p.q_s_tok = f.q.s_tok;
+    p.q_s_outer = f.q.s_outer;
     p.d = D;
     p.g = f.g;
     p.n_heads = f.n_heads;
@@ -394,7 +425,7 @@ cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
     const long n_qt = (f.q_len + kBM - 1) / kBM;
     const long items = n_qt * (long)f.n_heads * (long)f.n_outer;
     if (items == 0) return cudaSuccess;
-    kern<<<(unsigned)items, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+    kern<<<(unsigned)items, kThreads, C::kSmemBytes, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
