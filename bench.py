@@ -46,6 +46,29 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+# DRAM bytes (read + write) per launch at the 128K workload, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum; see
+# profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
+# sources they were taken on: a changed kernel reports null until re-measured.
+MEASURED_TRAFFIC = {
+    "attn_fwd": (129857717248 + 1058898688, "157d8610ff96950e", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (60683888640 + 530336768, "86059c6ba39c3480", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (236445761024 + 1051908096, "86059c6ba39c3480", ("attn_bwd.cu", "ptx.cuh")),
+}
+
+
+def measured_traffic(name: str, w):
+    import hashlib
+    if name not in MEASURED_TRAFFIC or w["N"] != 131072:
+        return None
+    nbytes, digest, files = MEASURED_TRAFFIC[name]
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "context_long_attention_ulysses_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest()[:16] == digest else None
+
+
 def causal_pairs(N: int) -> int:
     return N * (N + 1) // 2
 
@@ -363,7 +386,7 @@ def run_usp(args, world, rank, local):
             ach = work / (avg * 1e-3) / 1e12
             kernels[name] = {"bound": "tensor", "launches": launches, "ms_per_launch": avg, "achieved": ach,
                              "unit": "TFLOP/s", "frac_sustained": ach / peaks["bf16_sus"],
-                             "frac_burst": ach / peaks["bf16"]}
+                             "frac_burst": ach / peaks["bf16"], "traffic": measured_traffic(name, w)}
         else:
             ach = work / (avg * 1e-3) / 1e9
             kernels[name] = {"bound": "hbm", "launches": launches, "ms_per_launch": avg, "achieved": ach,
@@ -372,7 +395,7 @@ def run_usp(args, world, rank, local):
     dk = kernels[dom]
     if dk["bound"] == "tensor":
         roof = {"kernel": dom, "bound": "tensor", "achieved": dk["achieved"], "peak": peaks["bf16_sus"],
-                "unit": "TFLOP/s", "frac": dk["frac_sustained"], "traffic": None,
+                "unit": "TFLOP/s", "frac": dk["frac_sustained"], "traffic": dk.get("traffic"),
                 "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)"}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": dk["achieved"], "peak": peaks["hbm"], "unit": "GB/s",
