@@ -14,7 +14,7 @@
 //  1. pre:  D_i and lse_i*log2(e) into a workspace padded to 128-row tiles
 //           (padding rows: lse = +inf, so their P is exactly 0).
 //  2. dK/dV: one CTA per (KV head, 128-key tile).  It walks every query head
-//           of the GQA group and every 64-row query tile that sees its keys:
+//           of the GQA group and every 128-row query step that sees its keys:
 //             S^T  = K Q^T,  dP^T = V dO^T          (tcgen05, shared-memory operands)
 //             P^T, dS^T on CUDA cores (thread = key row = TMEM lane), bf16 into TMEM
 //             dV  += P^T dO, dK += dS^T Q           (A from TMEM, B MN-major)
@@ -22,10 +22,9 @@
 //  3. dQ:   one CTA per (query head, 128-row tile) walking its visible key
 //           tiles: S = Q K^T, dP = dO V^T, dS on CUDA cores into TMEM,
 //           dQ += dS K.
-// TMEM columns are laid out so that no MMA ever writes columns that another
-// MMA may still be reading: S/dP are single-buffered (the next S is issued
-// only after the softmax warps have loaded the previous one) and the bf16
-// operands P^T, dS^T (dS in pass 3) are double-buffered.
+// No MMA ever writes TMEM columns that an earlier-issued MMA still reads
+// unless it is issued after that MMA (tcgen05.mma executes in issue order);
+// each kernel's comment gives its column plan.
 #include <cmath>
 
 #include "kernels.h"
@@ -100,29 +99,44 @@ struct DevBwd {
 };
 
 // ------------------------------------------------------------------ pass 2: dK, dV
+// One 128-key tile per CTA, walked over 128-row query steps, so that every
+// product is a full 128 x 128 x 16 tcgen05.mma.  TMEM holds S^T, dP^T, dV and
+// dK (128 columns each); P^T and dS^T (bf16) are written in place over the
+// first half of each 64-column block of S^T and dP^T.  Per step the tensor
+// core runs
+//     S^T(i)  dP^T(i)  | dV(i)  S^T(i+1)  | dK(i)  dP^T(i+1) | dV(i+1) ...
+// and the element-wise warps compute P(i) while dP^T(i) runs and dS(i)
+// while dV(i) and S^T(i+1) run.  A product that overwrites S^T or dP^T is
+// issued after the one that reads the bf16 operand stored there
+// (tcgen05.mma executes in issue order).
+// Eight element-wise warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its
+// key rows) and query columns 64 (w / 4) .. + 63 of each step.
+constexpr int kKvEwWarps = 8;
+constexpr int kKvProducerWarp = 8;
+constexpr int kKvMmaWarp = 9;
+constexpr int kKvThreads = 10 * 32;
+
 template <int D>
 struct KvCfg {
     static constexpr int kBK = 128;  // keys per CTA (TMEM lanes)
-    static constexpr int kBQ = 64;   // query rows per step
+    static constexpr int kBQ = 128;  // query rows per step
     static constexpr int kChunks = D / 64;
-    static constexpr int kKVBytes = kChunks * kBK * 128;
-    static constexpr int kQBytes = kChunks * kBQ * 128;
-    static constexpr int kStages = 4;
-    static constexpr int kVecBytes = 2 * kBQ * 4;  // lse2 then dvec of one query tile
+    static constexpr int kTile = kChunks * 128 * 128;  // one 128-row bf16 tile (K, V, Q or dO)
+    static constexpr int kStages = 2;
+    static constexpr int kVecBytes = 2 * kBQ * 4;  // lse2 then dvec of one query step
     static constexpr int kOffK = 0;
-    static constexpr int kOffV = kKVBytes;
-    static constexpr int kOffQ = 2 * kKVBytes;
-    static constexpr int kOffDO = kOffQ + kStages * kQBytes;
-    static constexpr int kOffVec = kOffDO + kStages * kQBytes;
+    static constexpr int kOffV = kTile;
+    static constexpr int kOffQ = 2 * kTile;
+    static constexpr int kOffDO = kOffQ + kStages * kTile;
+    static constexpr int kOffVec = kOffDO + kStages * kTile;
     static constexpr int kOffBar = kOffVec + kStages * kVecBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1;
+    static constexpr int kNumBars = 1 + 2 * kStages + 5;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
-    static constexpr uint32_t kColS = 0, kColDP = 64, kColPt0 = 128, kColPt1 = 160, kColDSt0 = 192, kColDSt1 = 224,
-                              kColDV = 256, kColDK = 384;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
     using C = KvCfg<D>;
@@ -133,15 +147,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int abort_flag;
     const uint32_t bar0 = sbase + C::kOffBar;
     auto BAR = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
-    const int kKvFull = 0, kQFull = 1, kQEmpty = 1 + C::kStages, kSFull = 1 + 2 * C::kStages, kSFree = kSFull + 1,
-              kPReady = kSFree + 1, kOReady = kPReady + 2;
+    const int kKvFull = 0, kQFull = 1, kQEmpty = 1 + C::kStages, kSFull = 1 + 2 * C::kStages, kDPFull = kSFull + 1,
+              kPReady = kSFull + 2, kDSReady = kSFull + 3, kOReady = kSFull + 4;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int Zk = p.Zq / p.g;
     const int kt = blockIdx.x / Zk;  // low key tiles carry the most causal work: they go first
     const int zk = blockIdx.x % Zk;
     const int n_qt = (p.N + C::kBQ - 1) / C::kBQ;
-    const int qt_lo = p.causal ? (kt * C::kBK) / C::kBQ : 0;
+    const int qt_lo = p.causal ? kt : 0;  // kBQ == kBK: query steps before the diagonal see none of these keys
     const int nq = n_qt - qt_lo;
     const int n_it = p.g * nq;
 
@@ -153,13 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(kQEmpty + s), 1);
         }
         mbar_init(BAR(kSFull), 1);
-        mbar_init(BAR(kSFree), kSoftmaxWarps * 32);
-        mbar_init(BAR(kPReady), kSoftmaxWarps * 32);
-        mbar_init(BAR(kPReady + 1), kSoftmaxWarps * 32);
+        mbar_init(BAR(kDPFull), 1);
+        mbar_init(BAR(kPReady), kKvEwWarps * 32);
+        mbar_init(BAR(kDSReady), kKvEwWarps * 32);
         mbar_init(BAR(kOReady), 1);
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kKvMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -169,15 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     volatile int* abort_p = &abort_flag;
 
-    if (n_it > 0 && warp == kProducerWarp && lane == 0) {
+    if (n_it > 0 && warp == kKvProducerWarp && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_do);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(BAR(kKvFull), 2 * C::kKVBytes);
+        mbar_arrive_expect_tx(BAR(kKvFull), 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_4d(sbase + C::kOffK + c * (C::kBK * 128), &tm_k, c * 64, zk, kt * C::kBK, 0, BAR(kKvFull));
-            tma_load_4d(sbase + C::kOffV + c * (C::kBK * 128), &tm_v, c * 64, zk, kt * C::kBK, 0, BAR(kKvFull));
+            tma_load_4d(sbase + C::kOffK + c * 16384, &tm_k, c * 64, zk, kt * C::kBK, 0, BAR(kKvFull));
+            tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, zk, kt * C::kBK, 0, BAR(kKvFull));
         }
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::kStages;
@@ -186,148 +200,170 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it >= C::kStages &&
                 !mbar_wait(BAR(kQEmpty + s), ((it / C::kStages) - 1) & 1, abort_p, 21, p.status))
                 break;
-            mbar_arrive_expect_tx(BAR(kQFull + s), 2 * C::kQBytes + C::kVecBytes);
+            mbar_arrive_expect_tx(BAR(kQFull + s), 2 * C::kTile + C::kVecBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_4d(sbase + C::kOffQ + s * C::kQBytes + c * (C::kBQ * 128), &tm_q, c * 64, zq, qt * C::kBQ, 0,
+                tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, zq, qt * C::kBQ, 0,
                             BAR(kQFull + s));
-                tma_load_4d(sbase + C::kOffDO + s * C::kQBytes + c * (C::kBQ * 128), &tm_do, c * 64, zq, qt * C::kBQ,
-                            0, BAR(kQFull + s));
+                tma_load_4d(sbase + C::kOffDO + s * C::kTile + c * 16384, &tm_do, c * 64, zq, qt * C::kBQ, 0,
+                            BAR(kQFull + s));
             }
             const int64_t voff = (int64_t)zq * p.Npad + (int64_t)qt * C::kBQ;
             bulk_load(sbase + C::kOffVec + s * C::kVecBytes, p.lse2 + voff, C::kBQ * 4, BAR(kQFull + s));
             bulk_load(sbase + C::kOffVec + s * C::kVecBytes + C::kBQ * 4, p.dvec + voff, C::kBQ * 4, BAR(kQFull + s));
         }
-    } else if (n_it > 0 && warp == kMmaWarp && lane == 0) {
+    } else if (n_it > 0 && warp == kKvMmaWarp && lane == 0) {
         constexpr uint32_t kIdS = idesc_bf16(C::kBK, C::kBQ, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
         constexpr uint32_t kIdG = idesc_bf16(C::kBK, D, 0, 1);       // dV += P^T dO, dK += dS^T Q
         // descriptors built once; each k-step adds its offset (address field, 16-byte units)
         const uint64_t dk0 = sdesc_sw128(sbase + C::kOffK, 16, 1024), dv0 = sdesc_sw128(sbase + C::kOffV, 16, 1024);
-        auto issue_s = [&](int it) -> bool {
-            const int s = it % C::kStages;
-            if (!mbar_wait(BAR(kQFull + s), (it / C::kStages) & 1, abort_p, 22, p.status)) return false;
-            tc_fence_after();
-            const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ + s * C::kQBytes, 16, 1024);
-            const uint64_t ddo0 = sdesc_sw128(sbase + C::kOffDO + s * C::kQBytes, 16, 1024);
+        // S^T (A = K) or dP^T (A = V) of step it: B = Q or dO of its stage, both K-major
+        auto issue_t = [&](int it, uint64_t a0, int off_b, uint32_t col) {
+            const uint64_t b0 = sdesc_sw128(sbase + off_b + (it % C::kStages) * C::kTile, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t a_off = ((kk / 4) * (C::kBK * 128) + (kk % 4) * 32) >> 4;
-                const uint32_t b_off = ((kk / 4) * (C::kBQ * 128) + (kk % 4) * 32) >> 4;
-                mma_ss(tmem + C::kColS, dk0 + a_off, dq0 + b_off, kIdS, kk > 0);
+                const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                mma_ss(tmem + col, a0 + off, b0 + off, kIdS, kk > 0);
             }
+        };
+        // dV (A = P^T) or dK (A = dS^T) of step it: A from TMEM, B = dO or Q MN-major
+        auto issue_g = [&](int it, uint32_t col_a, int off_b, uint32_t col_d) {
+            const uint64_t b0 = sdesc_sw128(sbase + off_b + (it % C::kStages) * C::kTile, 16384, 1024);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t a_off = ((kk / 4) * (C::kBK * 128) + (kk % 4) * 32) >> 4;
-                const uint32_t b_off = ((kk / 4) * (C::kBQ * 128) + (kk % 4) * 32) >> 4;
-                mma_ss(tmem + C::kColDP, dv0 + a_off, ddo0 + b_off, kIdS, kk > 0);
+            for (int kk = 0; kk < C::kBQ / 16; ++kk) {
+                // queries 16 kk .. + 15 sit in the bf16 half of 64-column block kk / 4
+                const uint32_t a = tmem + col_a + (kk / 4) * 64 + (kk % 4) * 8;
+                mma_ts(tmem + col_d, a, b0 + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(BAR(kSFull));
-            return true;
         };
         bool ok = mbar_wait(BAR(kKvFull), 0, abort_p, 23, p.status);
-        ok = ok && issue_s(0);
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int s = it % C::kStages;
-            if (it + 1 < n_it) {
-                if (!mbar_wait(BAR(kSFree), it & 1, abort_p, 24, p.status)) break;
-                if (!issue_s(it + 1)) break;
-            }
-            if (!mbar_wait(BAR(kPReady + (it & 1)), (it >> 1) & 1, abort_p, 25, p.status)) break;
+        ok = ok && mbar_wait(BAR(kQFull), 0, abort_p, 22, p.status);
+        if (ok) {
             tc_fence_after();
-            const uint64_t bdo = sdesc_sw128(sbase + C::kOffDO + s * C::kQBytes, C::kBQ * 128, 1024);
-            const uint64_t bq = sdesc_sw128(sbase + C::kOffQ + s * C::kQBytes, C::kBQ * 128, 1024);
-            const uint32_t pt = tmem + ((it & 1) ? C::kColPt1 : C::kColPt0);
-            const uint32_t dst = tmem + ((it & 1) ? C::kColDSt1 : C::kColDSt0);
-#pragma unroll
-            for (int kk = 0; kk < C::kBQ / 16; ++kk)
-                mma_ts(tmem + C::kColDV, pt + kk * 8, bdo + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < C::kBQ / 16; ++kk)
-                mma_ts(tmem + C::kColDK, dst + kk * 8, bq + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(BAR(kQEmpty + s));
-            if (it + 1 == n_it) mma_commit(BAR(kOReady));
+            issue_t(0, dk0, C::kOffQ, C::kColS);
+            mma_commit(BAR(kSFull));
+            issue_t(0, dv0, C::kOffDO, C::kColDP);
+            mma_commit(BAR(kDPFull));
         }
-    } else if (warp < kSoftmaxWarps) {
+        for (int it = 0; ok && it < n_it; ++it) {
+            const bool more = it + 1 < n_it;
+            if (!mbar_wait(BAR(kPReady), it & 1, abort_p, 25, p.status)) break;
+            tc_fence_after();
+            issue_g(it, C::kColS, C::kOffDO, C::kColDV);
+            if (more) {
+                if (!mbar_wait(BAR(kQFull + (it + 1) % C::kStages), ((it + 1) / C::kStages) & 1, abort_p, 22,
+                               p.status))
+                    break;
+                tc_fence_after();
+                issue_t(it + 1, dk0, C::kOffQ, C::kColS);  // after dV(it), which read P^T from these columns
+                mma_commit(BAR(kSFull));
+            }
+            if (!mbar_wait(BAR(kDSReady), it & 1, abort_p, 24, p.status)) break;
+            tc_fence_after();
+            issue_g(it, C::kColDP, C::kOffQ, C::kColDK);
+            mma_commit(BAR(kQEmpty + it % C::kStages));
+            if (more) {
+                issue_t(it + 1, dv0, C::kOffDO, C::kColDP);  // after dK(it), which read dS^T from these columns
+                mma_commit(BAR(kDPFull));
+            } else {
+                mma_commit(BAR(kOReady));
+            }
+        }
+    } else if (warp < kKvEwWarps) {
         // ---------------------------------------------------------------- element-wise warps
-        const int c = threadIdx.x;  // key row within the tile = TMEM lane
-        const int key = kt * C::kBK + c;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int quad = warp & 3, half = warp >> 2;
+        const int key = kt * C::kBK + quad * 32 + lane;  // key row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t col_s = C::kColS + half * 64, col_dp = C::kColDP + half * 64;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::kStages;
             const int qt = qt_lo + it % nq;
+            // ---- P = exp2(S * scale * log2(e) - lse * log2(e)) on this warp's 64 query columns
             if (!mbar_wait(BAR(kSFull), it & 1, abort_p, 26, p.status)) { ok = false; break; }
             tc_fence_after();
-            uint32_t sa[32], sb[32], da[32], db[32];
-            tmem_ld32(lane_base + C::kColS, sa);
-            tmem_ld32(lane_base + C::kColS + 32, sb);
-            tmem_ld32(lane_base + C::kColDP, da);
-            tmem_ld32(lane_base + C::kColDP + 32, db);
+            uint32_t ra[32], rb[32];
+            tmem_ld32(lane_base + col_s, ra);
+            tmem_ld32(lane_base + col_s + 32, rb);
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(BAR(kSFree));
             if (!mbar_wait(BAR(kQFull + s), (it / C::kStages) & 1, abort_p, 27, p.status)) { ok = false; break; }
-            const float* vl = reinterpret_cast<const float*>(smem + C::kOffVec + s * C::kVecBytes);
+            const float* vl = reinterpret_cast<const float*>(smem + C::kOffVec + s * C::kVecBytes) + half * 64;
             const float* vd = vl + C::kBQ;
-            const int q0 = qt * C::kBQ;
+            const int q0 = qt * C::kBQ + half * 64;  // query of column 0
             const bool need_mask = p.causal && q0 < kt * C::kBK + C::kBK - 1;
             const int qmin_ok = key - q0;  // columns e with q0 + e >= key are visible
-            uint32_t pk[32], dk[32];
+            float pf[64];
+            uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < C::kBQ; e += 2) {
-                float sv0 = __uint_as_float(e < 32 ? sa[e] : sb[e - 32]);
-                float sv1 = __uint_as_float(e < 32 ? sa[e + 1] : sb[e - 31]);
-                float dp0 = __uint_as_float(e < 32 ? da[e] : db[e - 32]);
-                float dp1 = __uint_as_float(e < 32 ? da[e + 1] : db[e - 31]);
-                float p0 = ex2_approx(fmaf(sv0, p.scale_log2, -vl[e]));
-                float p1 = ex2_approx(fmaf(sv1, p.scale_log2, -vl[e + 1]));
-                if (need_mask) {
-                    if (e < qmin_ok) p0 = 0.f;
-                    if (e + 1 < qmin_ok) p1 = 0.f;
+            for (int e = 0; e < 64; e += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(vl + e);
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float sv = __uint_as_float(e + u < 32 ? ra[e + u] : rb[e + u - 32]);
+                    float pv = ex2_approx(fmaf(sv, p.scale_log2, -lv[u]));
+                    if (need_mask && e + u < qmin_ok) pv = 0.f;
+                    pf[e + u] = pv;
                 }
-                const float ds0 = p0 * (dp0 - vd[e]);
-                const float ds1 = p1 * (dp1 - vd[e + 1]);
-                pk[e / 2] = pack_bf16(p0, p1);
-                dk[e / 2] = pack_bf16(ds0, ds1);
+                pk[e / 2] = pack_bf16(pf[e], pf[e + 1]);
+                pk[e / 2 + 1] = pack_bf16(pf[e + 2], pf[e + 3]);
             }
-            const uint32_t pt = lane_base + ((it & 1) ? C::kColPt1 : C::kColPt0);
-            const uint32_t dst = lane_base + ((it & 1) ? C::kColDSt1 : C::kColDSt0);
-            tmem_st32(pt, pk);
-            tmem_st32(dst, dk);
+            tmem_st32(lane_base + col_s, pk);  // P^T over the first 32 of this warp's S^T columns
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(kPReady + (it & 1)));
+            mbar_arrive(BAR(kPReady));
+            // ---- dS = P (dP - D)
+            if (!mbar_wait(BAR(kDPFull), it & 1, abort_p, 28, p.status)) { ok = false; break; }
+            tc_fence_after();
+            tmem_ld32(lane_base + col_dp, ra);
+            tmem_ld32(lane_base + col_dp + 32, rb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+                const float4 d4 = *reinterpret_cast<const float4*>(vd + e);
+                const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                float ds[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float dp = __uint_as_float(e + u < 32 ? ra[e + u] : rb[e + u - 32]);
+                    ds[u] = pf[e + u] * (dp - dv4[u]);
+                }
+                pk[e / 2] = pack_bf16(ds[0], ds[1]);
+                pk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+            }
+            tmem_st32(lane_base + col_dp, pk);  // dS^T over the first 32 of this warp's dP^T columns
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(kDSReady));
         }
-        if (ok && n_it > 0) ok = mbar_wait(BAR(kOReady), 0, abort_p, 28, p.status);
+        if (ok && n_it > 0) ok = mbar_wait(BAR(kOReady), 0, abort_p, 29, p.status);
         if (ok) {
+            // warps 0-3 write dV, warps 4-7 write dK (scale applied here)
             tc_fence_after();
             const bool valid = key < p.N;
             const int64_t base = ((int64_t)zk * p.N + key) * D;
+            const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
+            const float mul = half == 0 ? 1.f : p.scale;
+            uint16_t* out = half == 0 ? p.dv : p.dk;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
-                const float mul = half == 0 ? 1.f : p.scale;
-                uint16_t* out = half == 0 ? p.dv : p.dk;
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t r[32];
+                if (n_it > 0) {
+                    tmem_ld32(lane_base + col + cc * 32, r);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    if (n_it > 0) {
-                        tmem_ld32(lane_base + col + cc * 32, r);
-                        tmem_wait_ld();
-                    } else {
+                    for (int e = 0; e < 32; ++e) r[e] = 0u;
+                }
+                if (valid) {
+                    uint4* dstp = reinterpret_cast<uint4*>(out + base + cc * 32);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = 0u;
-                    }
-                    if (valid) {
-                        uint4* dstp = reinterpret_cast<uint4*>(out + base + cc * 32);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint4 v;
-                            v.x = pack_bf16(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
-                            v.y = pack_bf16(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
-                            v.z = pack_bf16(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
-                            v.w = pack_bf16(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
-                            dstp[e] = v;
-                        }
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
+                        v.y = pack_bf16(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
+                        v.z = pack_bf16(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
+                        v.w = pack_bf16(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
+                        dstp[e] = v;
                     }
                 }
             }
@@ -335,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kKvMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -635,7 +671,7 @@ cudaError_t dkdv_t(const BwdParams& b, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int n_kt = (b.N + 127) / 128;
-    kern<<<(unsigned)(n_kt * (b.Zq / b.g)), kThreads, KvCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v,
+    kern<<<(unsigned)(n_kt * (b.Zq / b.g)), kKvThreads, KvCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v,
                                                                                       dev_params(b));
     return cudaGetLastError();
 }
