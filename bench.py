@@ -244,7 +244,8 @@ def kernel_work(name: str, w, launches: int):
     if name == "attn_bwd_dq":
         return "tensor", 1.5 * f               # S, dP, dQ: 6*d per visible pair
     if name == "attn_bwd_pre":
-        return "hbm", 2 * q_bytes + B * Hq * N * 4 + 2 * B * Hq * npad * 4
+        # reads O, dO and lse; writes D, lse*log2(e) (float32) and two 16-byte split rows per padded row
+        return "hbm", 2 * q_bytes + B * Hq * N * 4 + B * Hq * npad * (2 * 4 + 2 * 16)
     if name in ("a2a_seq2head", "a2a_head2seq"):
         # per step: Q, K, V, dO in (one launch each), O, dQ, dK, dV out; read + write bytes
         per_step = {"a2a_seq2head": 2 * (2 * q_bytes + 2 * kv_bytes),

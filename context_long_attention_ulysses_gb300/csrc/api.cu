@@ -257,9 +257,10 @@ usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, cons
 
 size_t usp_attn_bwd_workspace_size(const usp_problem* p) {
     if (check_problem(p) != USP_OK) return 0;
-    // D_i and lse_i*log2(e) per query row, rows padded to whole 128-row tiles
+    // per query row, rows padded to whole 128-row tiles: D_i and lse_i*log2(e) (float32), then
+    // -lse_i/scale and -D_i each as a 16-byte row of three bf16 numbers
     const size_t npad = ((size_t)p->N + 127) / 128 * 128;
-    return ((2 * (size_t)p->B * p->Hq * npad * sizeof(float)) + 255) & ~(size_t)255;
+    return (((size_t)p->B * p->Hq * npad * (2 * sizeof(float) + 2 * 16)) + 255) & ~(size_t)255;
 }
 
 usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,

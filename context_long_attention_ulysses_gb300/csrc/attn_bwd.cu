@@ -12,7 +12,9 @@
 //
 // Three launches, no atomics, deterministic:
 //  1. pre:  D_i and lse_i*log2(e) into a workspace padded to 128-row tiles
-//           (padding rows: lse = +inf, so their P is exactly 0).
+//           (padding rows: lse = +inf, so their P is exactly 0), and -lse_i/scale
+//           and -D_i each as a sum of three bf16 numbers: one extra k-step of
+//           the dK/dV products subtracts them (see pass 2).
 //  2. dK/dV: one CTA per (KV head, 128-key tile).  It walks every query head
 //           of the GQA group and every 128-row query step that sees its keys:
 //             S^T  = K Q^T,  dP^T = V dO^T          (tcgen05, shared-memory operands)
@@ -41,11 +43,25 @@ constexpr int kMmaWarp = 5;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ pass 1
-// One warp per padded row: dvec = dO . O (fp32), lse2 = lse * log2(e).
+// -x as three bf16 numbers a0 + a1 + a2 (each the rounded remainder of the
+// previous ones; together about 24 significant bits), packed as the 16-byte
+// row [a0, a1, a2, 0, 0, 0, 0, 0] that the dK/dV products' extra k-step reads.
+__device__ __forceinline__ float bf16_round(float x) { return __uint_as_float(pack_bf16(x, 0.f) << 16); }
+__device__ __forceinline__ uint4 neg_split3(float x) {
+    const float a0 = bf16_round(-x);
+    const float r1 = -x - a0;
+    const float a1 = bf16_round(r1);
+    const float a2 = bf16_round(r1 - a1);
+    return make_uint4(pack_bf16(a0, a1), pack_bf16(a2, 0.f), 0u, 0u);
+}
+
+// One warp per padded row: dvec = dO . O (fp32), lse2 = lse * log2(e), and
+// the split rows of lse / scale (xl) and of dvec (xd).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ dvec,
-                                                      float* __restrict__ lse2, int Zq, int N, int Npad) {
+                                                      float* __restrict__ lse2, uint4* __restrict__ xl,
+                                                      uint4* __restrict__ xd, float scale, int Zq, int N, int Npad) {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
     if (row >= (int64_t)Zq * Npad) return;
@@ -55,6 +71,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
         if (lane == 0) {
             dvec[row] = 0.f;
             lse2[row] = INFINITY;
+            xl[row] = make_uint4(0x0000FF7Fu, 0u, 0u, 0u);  // -(largest finite bf16): P underflows to 0
+            xd[row] = make_uint4(0u, 0u, 0u, 0u);
         }
         return;
     }
@@ -77,8 +95,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
+        const float l = lse[(int64_t)z * N + n];
         dvec[row] = acc;
-        lse2[row] = lse[(int64_t)z * N + n] * kLog2e;
+        lse2[row] = l * kLog2e;
+        xl[row] = neg_split3(l / scale);
+        xd[row] = neg_split3(acc);
     }
 }
 
@@ -94,6 +115,8 @@ struct DevBwd {
     float scale, scale_log2;
     const float* lse2;  // [Zq][Npad]
     const float* dvec;  // [Zq][Npad]
+    const uint4* xl;    // [Zq][Npad]: -lse / scale as three bf16 (a 16-byte row)
+    const uint4* xd;    // [Zq][Npad]: -D as three bf16
     uint16_t *dq, *dk, *dv;
     int* status;
 };
@@ -111,6 +134,14 @@ struct DevBwd {
 // (tcgen05.mma executes in issue order).
 // Eight element-wise warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its
 // key rows) and query columns 64 (w / 4) .. + 63 of each step.
+// The per-query values lse and D reach the element-wise warps through the
+// products rather than through per-element shared-memory loads: a ninth
+// k-step with A = a 128 x 16 tile of rows [1, 1, 1, 0, ...] and B = the
+// query rows of -lse/scale (resp. -D) split into three bf16 numbers leaves
+//     S'^T  = K Q^T - lse/scale      dP'^T = V dO^T - D
+// in TMEM, so that P = 2^(S' scale log2 e) and dS = P dP'.  Those small
+// operands are K-major without swizzle; the second 16-byte half of their
+// 32-byte rows (K = 16) is a shared block of zeros.
 constexpr int kKvEwWarps = 8;
 constexpr int kKvProducerWarp = 8;
 constexpr int kKvMmaWarp = 9;
@@ -123,13 +154,15 @@ struct KvCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTile = kChunks * 128 * 128;  // one 128-row bf16 tile (K, V, Q or dO)
     static constexpr int kStages = 2;
-    static constexpr int kVecBytes = 2 * kBQ * 4;  // lse2 then dvec of one query step
+    static constexpr int kXBytes = kBQ * 16;  // one 16-byte row per query: -lse/scale or -D as 3 bf16
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTile;
     static constexpr int kOffQ = 2 * kTile;
     static constexpr int kOffDO = kOffQ + kStages * kTile;
-    static constexpr int kOffVec = kOffDO + kStages * kTile;
-    static constexpr int kOffBar = kOffVec + kStages * kVecBytes;
+    static constexpr int kOffX = kOffDO + kStages * kTile;  // per stage: lse rows, then D rows
+    static constexpr int kOffOnes = kOffX + kStages * 2 * kXBytes;
+    static constexpr int kOffZero = kOffOnes + kBK * 16;
+    static constexpr int kOffBar = kOffZero + 2048;
     static constexpr int kNumBars = 1 + 2 * kStages + 5;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -177,6 +210,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
+    if (threadIdx.x < C::kBK) {
+        // row t of the ones operand (bf16 1.0 = 0x3F80 in its first three columns) and 16 bytes of zeros
+        *reinterpret_cast<uint4*>(smem + C::kOffOnes + threadIdx.x * 16) = make_uint4(0x3F803F80u, 0x3F80u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + C::kOffZero + threadIdx.x * 16) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -200,7 +239,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             if (it >= C::kStages &&
                 !mbar_wait(BAR(kQEmpty + s), ((it / C::kStages) - 1) & 1, abort_p, 21, p.status))
                 break;
-            mbar_arrive_expect_tx(BAR(kQFull + s), 2 * C::kTile + C::kVecBytes);
+            mbar_arrive_expect_tx(BAR(kQFull + s), 2 * C::kTile + 2 * C::kXBytes);
             for (int c = 0; c < C::kChunks; ++c) {
                 tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, zq, qt * C::kBQ, 0,
                             BAR(kQFull + s));
@@ -208,22 +247,31 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                             BAR(kQFull + s));
             }
             const int64_t voff = (int64_t)zq * p.Npad + (int64_t)qt * C::kBQ;
-            bulk_load(sbase + C::kOffVec + s * C::kVecBytes, p.lse2 + voff, C::kBQ * 4, BAR(kQFull + s));
-            bulk_load(sbase + C::kOffVec + s * C::kVecBytes + C::kBQ * 4, p.dvec + voff, C::kBQ * 4, BAR(kQFull + s));
+            bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes, p.xl + voff, C::kXBytes, BAR(kQFull + s));
+            bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes + C::kXBytes, p.xd + voff, C::kXBytes, BAR(kQFull + s));
         }
     } else if (n_it > 0 && warp == kKvMmaWarp && lane == 0) {
         constexpr uint32_t kIdS = idesc_bf16(C::kBK, C::kBQ, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
         constexpr uint32_t kIdG = idesc_bf16(C::kBK, D, 0, 1);       // dV += P^T dO, dK += dS^T Q
         // descriptors built once; each k-step adds its offset (address field, 16-byte units)
         const uint64_t dk0 = sdesc_sw128(sbase + C::kOffK, 16, 1024), dv0 = sdesc_sw128(sbase + C::kOffV, 16, 1024);
-        // S^T (A = K) or dP^T (A = V) of step it: B = Q or dO of its stage, both K-major
-        auto issue_t = [&](int it, uint64_t a0, int off_b, uint32_t col) {
-            const uint64_t b0 = sdesc_sw128(sbase + off_b + (it % C::kStages) * C::kTile, 16, 1024);
+        // the extra k-step's operands: rows of ones (A) and the stage's split rows (B); 8-row
+        // groups 128 bytes apart, the zero half of every row at the shared zero block
+        auto plain = [&](int off) {
+            return sdesc_plain(sbase + off, (uint32_t)(C::kOffZero - off), 128);
+        };
+        const uint64_t dones = plain(C::kOffOnes);
+        // S'^T (A = K, x = 0: lse rows) or dP'^T (A = V, x = 1: D rows) of step it: B = Q or dO of
+        // its stage, both K-major
+        auto issue_t = [&](int it, uint64_t a0, int off_b, uint32_t col, int x) {
+            const int s = it % C::kStages;
+            const uint64_t b0 = sdesc_sw128(sbase + off_b + s * C::kTile, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
                 mma_ss(tmem + col, a0 + off, b0 + off, kIdS, kk > 0);
             }
+            mma_ss(tmem + col, dones, plain(C::kOffX + (2 * s + x) * C::kXBytes), kIdS, 1u);
         };
         // dV (A = P^T) or dK (A = dS^T) of step it: A from TMEM, B = dO or Q MN-major
         auto issue_g = [&](int it, uint32_t col_a, int off_b, uint32_t col_d) {
@@ -239,9 +287,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         ok = ok && mbar_wait(BAR(kQFull), 0, abort_p, 22, p.status);
         if (ok) {
             tc_fence_after();
-            issue_t(0, dk0, C::kOffQ, C::kColS);
+            issue_t(0, dk0, C::kOffQ, C::kColS, 0);
             mma_commit(BAR(kSFull));
-            issue_t(0, dv0, C::kOffDO, C::kColDP);
+            issue_t(0, dv0, C::kOffDO, C::kColDP, 1);
             mma_commit(BAR(kDPFull));
         }
         for (int it = 0; ok && it < n_it; ++it) {
@@ -254,7 +302,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                                p.status))
                     break;
                 tc_fence_after();
-                issue_t(it + 1, dk0, C::kOffQ, C::kColS);  // after dV(it), which read P^T from these columns
+                issue_t(it + 1, dk0, C::kOffQ, C::kColS, 0);  // after dV(it), which read P^T from these columns
                 mma_commit(BAR(kSFull));
             }
             if (!mbar_wait(BAR(kDSReady), it & 1, abort_p, 24, p.status)) break;
@@ -262,7 +310,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             issue_g(it, C::kColDP, C::kOffQ, C::kColDK);
             mma_commit(BAR(kQEmpty + it % C::kStages));
             if (more) {
-                issue_t(it + 1, dv0, C::kOffDO, C::kColDP);  // after dK(it), which read dS^T from these columns
+                issue_t(it + 1, dv0, C::kOffDO, C::kColDP, 1);  // after dK(it), which read dS^T from these columns
                 mma_commit(BAR(kDPFull));
             } else {
                 mma_commit(BAR(kOReady));
@@ -276,7 +324,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t col_s = C::kColS + half * 64, col_dp = C::kColDP + half * 64;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int s = it % C::kStages;
             const int qt = qt_lo + it % nq;
             // ---- P = exp2(S * scale * log2(e) - lse * log2(e)) on this warp's 64 query columns
             if (!mbar_wait(BAR(kSFull), it & 1, abort_p, 26, p.status)) { ok = false; break; }
@@ -285,27 +332,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tmem_ld32(lane_base + col_s, ra);
             tmem_ld32(lane_base + col_s + 32, rb);
             tmem_wait_ld();
-            if (!mbar_wait(BAR(kQFull + s), (it / C::kStages) & 1, abort_p, 27, p.status)) { ok = false; break; }
-            const float* vl = reinterpret_cast<const float*>(smem + C::kOffVec + s * C::kVecBytes) + half * 64;
-            const float* vd = vl + C::kBQ;
             const int q0 = qt * C::kBQ + half * 64;  // query of column 0
             const bool need_mask = p.causal && q0 < kt * C::kBK + C::kBK - 1;
             const int qmin_ok = key - q0;  // columns e with q0 + e >= key are visible
             float pf[64];
             uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const float4 l4 = *reinterpret_cast<const float4*>(vl + e);
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            for (int e = 0; e < 64; e += 2) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 2; ++u) {
                     const float sv = __uint_as_float(e + u < 32 ? ra[e + u] : rb[e + u - 32]);
-                    float pv = ex2_approx(fmaf(sv, p.scale_log2, -lv[u]));
+                    float pv = ex2_approx(sv * p.scale_log2);  // S' already holds S - lse / scale
                     if (need_mask && e + u < qmin_ok) pv = 0.f;
                     pf[e + u] = pv;
                 }
                 pk[e / 2] = pack_bf16(pf[e], pf[e + 1]);
-                pk[e / 2 + 1] = pack_bf16(pf[e + 2], pf[e + 3]);
             }
             tmem_st32(lane_base + col_s, pk);  // P^T over the first 32 of this warp's S^T columns
             tmem_wait_st();
@@ -318,17 +359,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tmem_ld32(lane_base + col_dp + 32, rb);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const float4 d4 = *reinterpret_cast<const float4*>(vd + e);
-                const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                float ds[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float dp = __uint_as_float(e + u < 32 ? ra[e + u] : rb[e + u - 32]);
-                    ds[u] = pf[e + u] * (dp - dv4[u]);
-                }
-                pk[e / 2] = pack_bf16(ds[0], ds[1]);
-                pk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+            for (int e = 0; e < 64; e += 2) {
+                // dP' already holds dP - D
+                const float ds0 = pf[e] * __uint_as_float(e < 32 ? ra[e] : rb[e - 32]);
+                const float ds1 = pf[e + 1] * __uint_as_float(e + 1 < 32 ? ra[e + 1] : rb[e - 31]);
+                pk[e / 2] = pack_bf16(ds0, ds1);
             }
             tmem_st32(lane_base + col_dp, pk);  // dS^T over the first 32 of this warp's dP^T columns
             tmem_wait_st();
@@ -646,6 +681,8 @@ DevBwd dev_params(const BwdParams& b) {
     p.scale_log2 = b.scale * kLog2e;
     p.dvec = b.dvec;
     p.lse2 = b.dvec + (size_t)b.Zq * Npad;
+    p.xl = reinterpret_cast<const uint4*>(b.dvec + 2 * (size_t)b.Zq * Npad);
+    p.xd = p.xl + (size_t)b.Zq * Npad;
     p.dq = static_cast<uint16_t*>(b.dq);
     p.dk = static_cast<uint16_t*>(b.dk);
     p.dv = static_cast<uint16_t*>(b.dv);
@@ -659,7 +696,7 @@ cudaError_t pre_t(const BwdParams& b, cudaStream_t stream) {
     const int64_t rows = (int64_t)b.Zq * p.Npad;
     bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
         static_cast<const uint16_t*>(b.o), static_cast<const uint16_t*>(b.dout), b.lse, const_cast<float*>(p.dvec),
-        const_cast<float*>(p.lse2), b.Zq, b.N, p.Npad);
+        const_cast<float*>(p.lse2), const_cast<uint4*>(p.xl), const_cast<uint4*>(p.xd), b.scale, b.Zq, b.N, p.Npad);
     return cudaGetLastError();
 }
 

@@ -61,7 +61,8 @@ cudaError_t launch_attn_fwd_bf16(const FwdParams& p, cudaStream_t stream);
 struct BwdParams {
     const void *q, *k, *v, *o, *dout;
     const float* lse;
-    float* dvec;  // workspace base: D_i = dO_i . O_i, then lse_i*log2(e), [Zq][Npad] each
+    float* dvec;  // workspace base: D_i = dO_i . O_i, then lse_i*log2(e), [Zq][Npad] each (float32),
+                  // then -lse_i/scale and -D_i as 16-byte rows of three bf16, [Zq][Npad] each
     void *dq, *dk, *dv;
     int Zq, g, N, d, causal;
     float scale;

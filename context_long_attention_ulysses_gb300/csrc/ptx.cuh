@@ -196,6 +196,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// Descriptor of a K-major operand without swizzle (layout type 0): 8-row x
+// 16-byte core matrices, consecutive 8-row groups sbo_bytes apart, the two
+// 16-byte halves of a 32-byte (K = 16 bf16) row lbo_bytes apart.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Make this thread's generic-proxy writes to shared memory visible to the
+// async proxy (tensor core operand reads, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 D.
 // a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

@@ -118,9 +118,10 @@ usp_status usp_a2a_head2seq(const usp_problem* p, int Hx, const void* src, void*
 usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
                         float* lse, usp_stream stream);
 
-/* Bytes of workspace usp_attn_bwd needs: linear in N (two float32 per query
- * row -- D_i and lse_i*log2(e) -- with rows padded to 128-row tiles), never
- * quadratic.  Returns 0 for an invalid problem. */
+/* Bytes of workspace usp_attn_bwd needs: linear in N, never quadratic: 40
+ * bytes per query row, rows padded to 128-row tiles (D_i and lse_i*log2(e)
+ * as float32, and -lse_i/scale and -D_i each as three bf16 numbers in a
+ * 16-byte row).  Returns 0 for an invalid problem. */
 size_t usp_attn_bwd_workspace_size(const usp_problem* p);
 
 /* Attention backward on head-sharded buffers (the backward of the glossary
@@ -138,8 +139,8 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
                         size_t ws_bytes, usp_stream stream);
 
 /* Size of the scratch array built into the library for
- * usp_attn_bwd_noalloc: 64 MiB, enough for B*Hq*roundup(N,128) <= 8 Mi query
- * rows (e.g. 32 heads of 262 144 tokens). */
+ * usp_attn_bwd_noalloc: 64 MiB, enough for B*Hq*roundup(N,128) <= 1.6 Mi
+ * query rows at 40 bytes each (e.g. 32 heads of 49 152 tokens). */
 #define USP_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /* usp_attn_bwd for callers that cannot allocate device memory -- code inside

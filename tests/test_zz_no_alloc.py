@@ -22,7 +22,7 @@ def usp():
 
 
 def test_rejects_problems_larger_than_the_scratch(usp):
-    # needs 2 * 4 bytes * 32 heads * 524288 rows = 128 MiB > the built-in 64 MiB; refused before any CUDA call
+    # needs 40 bytes * 32 heads * 524288 rows = 640 MiB > the built-in 64 MiB; refused before any CUDA call
     p = usp.Problem(B=1, Hq=32, Hkv=8, N=524288, d=128, P=8)
     assert usp.usp_attn_bwd_workspace_size(p) > usp.NOALLOC_SCRATCH_BYTES
     fake = 1 << 20
