@@ -36,10 +36,6 @@ namespace usp {
 
 namespace {
 
-constexpr int kThreads = 6 * 32;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ pass 1
@@ -414,6 +410,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ------------------------------------------------------------------ pass 3: dQ
+// Eight element-wise warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its
+// query rows) and key columns 64 (w / 4) .. + 63 of each step, so two warps
+// share each sub-partition and hide each other's latency.
+constexpr int kDqEwWarps = 8;
+constexpr int kDqProducerWarp = 8;
+constexpr int kDqMmaWarp = 9;
+constexpr int kDqThreads = 10 * 32;
+
 template <int D>
 struct DqCfg {
     static constexpr int kBM = 128;  // query rows per CTA (TMEM lanes)
@@ -434,7 +438,7 @@ struct DqCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
     using C = DqCfg<D>;
@@ -469,13 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(kVEmpty + s), 1);
         }
         mbar_init(BAR(kSFull), 1);
-        mbar_init(BAR(kSFree), kSoftmaxWarps * 32);
-        mbar_init(BAR(kDsReady), kSoftmaxWarps * 32);
-        mbar_init(BAR(kDsReady + 1), kSoftmaxWarps * 32);
+        mbar_init(BAR(kSFree), kDqEwWarps * 32);
+        mbar_init(BAR(kDsReady), kDqEwWarps * 32);
+        mbar_init(BAR(kDsReady + 1), kDqEwWarps * 32);
         mbar_init(BAR(kOReady), 1);
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kDqMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     volatile int* abort_p = &abort_flag;
 
-    if (n_it > 0 && warp == kProducerWarp && lane == 0) {
+    if (n_it > 0 && warp == kDqProducerWarp && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_do);
         tma_prefetch_desc(&tm_k);
@@ -512,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sbase + C::kOffV + vs * C::kTile + c * 16384, &tm_v, c * 64, zk, j * C::kBN, 0,
                             BAR(kVFull + vs));
         }
-    } else if (n_it > 0 && warp == kMmaWarp && lane == 0) {
+    } else if (n_it > 0 && warp == kDqMmaWarp && lane == 0) {
         constexpr uint32_t kIdS = idesc_bf16(C::kBM, C::kBN, 0, 0);  // S = Q K^T, dP = dO V^T
         constexpr uint32_t kIdG = idesc_bf16(C::kBM, D, 0, 1);       // dQ += dS K, K MN-major
         // descriptors built once; each k-step adds its offset (address field, 16-byte units)
@@ -556,10 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(BAR(kKEmpty + ks));
             if (j + 1 == n_it) mma_commit(BAR(kOReady));
         }
-    } else if (warp < kSoftmaxWarps) {
-        const int r = threadIdx.x;  // query row within the tile = TMEM lane
+    } else if (warp < kDqEwWarps) {
+        const int quad = warp & 3, half = warp >> 2;
+        const int r = quad * 32 + lane;  // query row within the tile = TMEM lane
         const int q = qt * C::kBM + r;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const int64_t vrow = (int64_t)zq * p.Npad + q;  // q < Npad always
         const float lse2_r = p.lse2[vrow];
         const float dv_r = p.dvec[vrow];
@@ -567,63 +572,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n_it; ++j) {
             if (!mbar_wait(BAR(kSFull), j & 1, abort_p, 36, p.status)) { ok = false; break; }
             tc_fence_after();
-            const int key0 = j * C::kBN;
+            const int key0 = j * C::kBN + half * 64;  // key of this warp's column 0
             // visible columns: key0 + c <= q (causal) and key0 + c < N
             int climit = p.N - 1 - key0;
             if (p.causal) climit = min(climit, q - key0);
-            const bool need_mask = climit < C::kBN - 1;
-            uint32_t dsp[64];
+            const bool need_mask = climit < 63;
+            uint32_t sa[32], sb[32], da[32], db[32];
+            tmem_ld32(lane_base + C::kColS + half * 64, sa);
+            tmem_ld32(lane_base + C::kColS + half * 64 + 32, sb);
+            tmem_ld32(lane_base + C::kColDP + half * 64, da);
+            tmem_ld32(lane_base + C::kColDP + half * 64 + 32, db);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(BAR(kSFree));  // S and dP of step j are in registers: the next products may start
+            uint32_t dsp[32];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sa[32], sb[32], da[32], db[32];
-                tmem_ld32(lane_base + C::kColS + half * 64, sa);
-                tmem_ld32(lane_base + C::kColS + half * 64 + 32, sb);
-                tmem_ld32(lane_base + C::kColDP + half * 64, da);
-                tmem_ld32(lane_base + C::kColDP + half * 64 + 32, db);
-                tmem_wait_ld();
-                if (half == 1) {
-                    tc_fence_before();
-                    mbar_arrive(BAR(kSFree));
+            for (int e = 0; e < 64; e += 2) {
+                const float sv0 = __uint_as_float(e < 32 ? sa[e] : sb[e - 32]);
+                const float sv1 = __uint_as_float(e < 32 ? sa[e + 1] : sb[e - 31]);
+                const float dp0 = __uint_as_float(e < 32 ? da[e] : db[e - 32]);
+                const float dp1 = __uint_as_float(e < 32 ? da[e + 1] : db[e - 31]);
+                float p0 = ex2_approx(fmaf(sv0, p.scale_log2, -lse2_r));
+                float p1 = ex2_approx(fmaf(sv1, p.scale_log2, -lse2_r));
+                if (need_mask) {
+                    if (e > climit) p0 = 0.f;
+                    if (e + 1 > climit) p1 = 0.f;
                 }
-#pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const int col = half * 64 + e;
-                    const float sv0 = __uint_as_float(e < 32 ? sa[e] : sb[e - 32]);
-                    const float sv1 = __uint_as_float(e < 32 ? sa[e + 1] : sb[e - 31]);
-                    const float dp0 = __uint_as_float(e < 32 ? da[e] : db[e - 32]);
-                    const float dp1 = __uint_as_float(e < 32 ? da[e + 1] : db[e - 31]);
-                    float p0 = ex2_approx(fmaf(sv0, p.scale_log2, -lse2_r));
-                    float p1 = ex2_approx(fmaf(sv1, p.scale_log2, -lse2_r));
-                    if (need_mask) {
-                        if (col > climit) p0 = 0.f;
-                        if (col + 1 > climit) p1 = 0.f;
-                    }
-                    dsp[half * 32 + e / 2] = pack_bf16(p0 * (dp0 - dv_r), p1 * (dp1 - dv_r));
-                }
+                dsp[e / 2] = pack_bf16(p0 * (dp0 - dv_r), p1 * (dp1 - dv_r));
             }
-            const uint32_t ds = lane_base + ((j & 1) ? C::kColDS1 : C::kColDS0);
-            uint32_t lo[32], hi[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                lo[e] = dsp[e];
-                hi[e] = dsp[32 + e];
-            }
-            tmem_st32(ds, lo);
-            tmem_st32(ds + 32, hi);
+            // dS (bf16) of keys 64 half .. + 63 into columns 32 half .. + 31 of this step's buffer
+            tmem_st32(lane_base + ((j & 1) ? C::kColDS1 : C::kColDS0) + half * 32, dsp);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(kDsReady + (j & 1)));
         }
         if (ok && n_it > 0) ok = mbar_wait(BAR(kOReady), 0, abort_p, 37, p.status);
         if (ok) {
+            // each warp writes half of the row's dQ columns
             tc_fence_after();
             const bool valid = q < p.N;
-            const int64_t base = ((int64_t)zq * p.N + q) * D;
+            const int64_t base = ((int64_t)zq * p.N + q) * D + half * (D / 2);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t rr[32];
                 if (n_it > 0) {
-                    tmem_ld32(lane_base + C::kColDQ + cc * 32, rr);
+                    tmem_ld32(lane_base + C::kColDQ + half * (D / 2) + cc * 32, rr);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -646,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kDqMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -721,7 +714,7 @@ cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int n_qt = (b.N + 127) / 128;
-    kern<<<(unsigned)(n_qt * b.Zq), kThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
+    kern<<<(unsigned)(n_qt * b.Zq), kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
     return cudaGetLastError();
 }
 
