@@ -51,9 +51,9 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
 # sources they were taken on: a changed kernel reports null until re-measured.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (129857717248 + 1058898688, "157d8610ff96950e", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (60683888640 + 530336768, "86059c6ba39c3480", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (236445761024 + 1051908096, "86059c6ba39c3480", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (40999906560 + 1285327360, "0b29a310bddc8634", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (63177362432 + 528116736, "aad40e7f33180e22", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (81208904192 + 1051179008, "aad40e7f33180e22", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 
@@ -495,7 +495,7 @@ def main():
     ap.add_argument("--impl", choices=["usp", "reference"], default="usp")
     ap.add_argument("--no-ring", dest="ring", action="store_false", help="skip the 512K ring measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows per head for cpu_baseline")
+    ap.add_argument("--cpu-rows", type=int, default=144, help="oracle rows per head for cpu_baseline")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="128k")
     args = ap.parse_args()
     global WORKLOAD, WORKLOAD_NAME
