@@ -29,6 +29,7 @@ SYMBOLS = (
     "usp_a2a_seq2head", "usp_a2a_head2seq", "usp_attn_fwd", "usp_attn_bwd_workspace_size", "usp_attn_bwd",
     "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
     "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "usp_attn_bwd_noalloc",
+    "usp_ring_bwd_workspace_size", "usp_ring_attn_bwd",
 )
 
 
@@ -86,6 +87,8 @@ def load() -> ctypes.CDLL:
             "usp_trace_reset": (ci, []),
             "usp_trace_report": (ci, [ctypes.POINTER(UspTraceEntry), ci]),
             "usp_attn_bwd_noalloc": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "usp_ring_bwd_workspace_size": (sz, [P]),
+            "usp_ring_attn_bwd": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

@@ -278,15 +278,26 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
     if (ws_bytes < usp_attn_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
     int* sp = status_ptr();
     if (!sp) return USP_ERR_CUDA;
+    // head-sharded buffers as Z = B*Hq query heads (Z/g KV heads) of N tokens, one outer index
+    const int Z = p->B * p->Hq, Zk = p->B * p->Hkv, d = p->d, N = p->N;
+    const int64_t nd = (int64_t)N * d;
     BwdParams b{};
-    b.q = q; b.k = k; b.v = v; b.o = o; b.dout = dout; b.lse = lse;
-    b.dvec = static_cast<float*>(ws);
+    b.q = Tensor4{const_cast<void*>(q), nd, d, nd * Z, Z, N, 1};
+    b.o = Tensor4{const_cast<void*>(o), nd, d, nd * Z, Z, N, 1};
+    b.dout = Tensor4{const_cast<void*>(dout), nd, d, nd * Z, Z, N, 1};
+    b.k = Tensor4{const_cast<void*>(k), nd, d, nd * Zk, Zk, N, 1};
+    b.v = Tensor4{const_cast<void*>(v), nd, d, nd * Zk, Zk, N, 1};
+    b.lse = lse;
+    b.l_s_head = N;
+    b.l_s_tok = 1;
+    b.l_s_outer = (int64_t)Z * N;
+    b.ws = static_cast<float*>(ws);
+    b.n_z = Z;
     b.dq = dq; b.dk = dk; b.dv = dv;
-    b.Zq = p->B * p->Hq;
+    b.d = d;
     b.g = p->Hq / p->Hkv;
-    b.N = p->N;
-    b.d = p->d;
     b.causal = p->causal ? 1 : 0;
+    b.ring_i0 = 0; b.ring_t = 0; b.ring_p = 1; b.bsz = 1; b.n_outer = 1;
     b.scale = eff_scale(p);
     b.status = sp;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -384,6 +395,91 @@ usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k,
         }
     }
     return cuda_status(traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s); }));
+}
+
+// Ring backward workspace: the backward rows (40 bytes per padded query row
+// of every rank and head: D, lse*log2(e), -lse/scale and -D as bf16 splits),
+// then float32 accumulators for dQ, dK and dV in sequence-sharded order.
+static size_t ring_bwd_rows(const usp_problem* p) {
+    const size_t npad = ((size_t)(p->N / p->P) + 127) / 128 * 128;
+    return (size_t)p->P * p->B * p->Hq * npad;
+}
+
+size_t usp_ring_bwd_workspace_size(const usp_problem* p) {
+    if (check_problem(p, false) != USP_OK) return 0;
+    const size_t q_elems = (size_t)p->B * p->N * p->Hq * p->d, k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
+    return ring_part(ring_bwd_rows(p) * 40) + ring_part(q_elems * 4) + 2 * ring_part(k_elems * 4);
+}
+
+usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                             size_t ws_bytes, usp_stream stream) {
+    usp_status st = check_problem(p, false);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
+    if ((int64_t)p->B * p->P > 65535) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    if (ws_bytes < usp_ring_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d;
+    const int Np = p->N / P;
+    const size_t q_elems = (size_t)B * p->N * Hq * d, k_elems = (size_t)B * p->N * Hkv * d;
+    char* w = static_cast<char*>(ws);
+    float* acc_dq = reinterpret_cast<float*>(w + ring_part(ring_bwd_rows(p) * 40));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(q_elems * 4));
+    float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(k_elems * 4));
+
+    BwdParams b{};
+    const int64_t qs_tok = (int64_t)Hq * d, ks_tok = (int64_t)Hkv * d;
+    b.q = Tensor4{const_cast<void*>(q), d, qs_tok, (int64_t)Np * qs_tok, Hq, Np, P * B};
+    b.o = Tensor4{const_cast<void*>(o), d, qs_tok, (int64_t)Np * qs_tok, Hq, Np, P * B};
+    b.dout = Tensor4{const_cast<void*>(dout), d, qs_tok, (int64_t)Np * qs_tok, Hq, Np, P * B};
+    b.k = Tensor4{const_cast<void*>(k), d, ks_tok, (int64_t)Np * ks_tok, Hkv, Np, P * B};
+    b.v = Tensor4{const_cast<void*>(v), d, ks_tok, (int64_t)Np * ks_tok, Hkv, Np, P * B};
+    b.lse = lse;  // [P][B][N/P][Hq], the merged LSE of usp_ring_attn_fwd
+    b.l_s_head = 1;
+    b.l_s_tok = Hq;
+    b.l_s_outer = (int64_t)Np * Hq;
+    b.ws = reinterpret_cast<float*>(w);
+    b.n_z = P * B * Hq;
+    b.dq_f32 = acc_dq;
+    b.dk_f32 = acc_dk;
+    b.dv_f32 = acc_dv;
+    b.d = d;
+    b.g = Hq / Hkv;
+    b.ring_p = P;
+    b.bsz = B;
+    b.scale = eff_scale(p);
+    b.status = sp;
+
+    // D and the lse rows of every rank (they use the final O and the merged LSE)
+    cudaError_t e = traced("ring_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
+    if (e != cudaSuccess) return USP_ERR_CUDA;
+    for (int t = 0; t < P; ++t) {
+        // step t: rank i holds KV block j = (i - t) mod P (skipped when j > i under the causal mask,
+        // masked only when j == i); its dK_j, dV_j partials travel with the block, dQ_i stays on rank i.
+        // Every block receives its first contribution at t = 0, so later steps add.
+        b.ring_t = t;
+        b.ring_i0 = p->causal ? t : 0;
+        b.n_outer = (p->causal ? P - t : P) * B;
+        b.causal = (p->causal && t == 0) ? 1 : 0;
+        b.accumulate = t > 0 ? 1 : 0;
+        e = traced("ring_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+        if (e == cudaSuccess) e = traced("ring_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
+        if (e != cudaSuccess) return USP_ERR_CUDA;
+    }
+    e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dq, dq, (int64_t)q_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dk, dk, (int64_t)k_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dv, dv, (int64_t)k_elems, s); });
+    return cuda_status(e);
 }
 
 usp_status usp_trace_enable(int on) {

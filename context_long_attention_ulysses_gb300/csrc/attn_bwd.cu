@@ -51,18 +51,34 @@ __device__ __forceinline__ uint4 neg_split3(float x) {
     return make_uint4(pack_bf16(a0, a1), pack_bf16(a2, 0.f), 0u, 0u);
 }
 
-// One warp per padded row: dvec = dO . O (fp32), lse2 = lse * log2(e), and
-// the split rows of lse / scale (xl) and of dvec (xd).
+struct PreArgs {
+    const uint16_t* o;     // shaped and strided as q
+    const uint16_t* dout;  // likewise
+    const float* lse;
+    int64_t s_head, s_tok, s_outer;        // o / dout strides (elements)
+    int64_t l_s_head, l_s_tok, l_s_outer;  // lse strides
+    int heads, N, Npad, n_z;
+    float scale;
+    float *dvec, *lse2;
+    uint4 *xl, *xd;
+};
+
+// One warp per padded row z * Npad + n (z = outer * heads + head): dvec = dO . O
+// (fp32), lse2 = lse * log2(e), and the split rows of lse / scale (xl) and of
+// dvec (xd).
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                      const float* __restrict__ lse, float* __restrict__ dvec,
-                                                      float* __restrict__ lse2, uint4* __restrict__ xl,
-                                                      uint4* __restrict__ xd, float scale, int Zq, int N, int Npad) {
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
-    if (row >= (int64_t)Zq * Npad) return;
-    const int z = (int)(row / Npad);
-    const int n = (int)(row % Npad);
+    if (row >= (int64_t)a.n_z * a.Npad) return;
+    const int z = (int)(row / a.Npad);
+    const int n = (int)(row % a.Npad);
+    const int outer = z / a.heads, head = z % a.heads;
+    float* __restrict__ dvec = a.dvec;
+    float* __restrict__ lse2 = a.lse2;
+    uint4* __restrict__ xl = a.xl;
+    uint4* __restrict__ xd = a.xd;
+    const int N = a.N;
     if (n >= N) {
         if (lane == 0) {
             dvec[row] = 0.f;
@@ -73,7 +89,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
         return;
     }
     constexpr int kPer = D / 32;  // elements per lane (2 or 4)
-    const int64_t base = ((int64_t)z * N + n) * D + lane * kPer;
+    const int64_t base = (int64_t)outer * a.s_outer + (int64_t)head * a.s_head + (int64_t)n * a.s_tok + lane * kPer;
+    const uint16_t* __restrict__ o = a.o;
+    const uint16_t* __restrict__ dout = a.dout;
     float acc = 0.f;
     if constexpr (kPer == 4) {
         const uint2 a = *reinterpret_cast<const uint2*>(o + base);
@@ -91,10 +109,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-        const float l = lse[(int64_t)z * N + n];
+        const float l = a.lse[(int64_t)outer * a.l_s_outer + (int64_t)head * a.l_s_head + (int64_t)n * a.l_s_tok];
         dvec[row] = acc;
         lse2[row] = l * kLog2e;
-        xl[row] = neg_split3(l / scale);
+        xl[row] = neg_split3(l / a.scale);
         xd[row] = neg_split3(acc);
     }
 }
@@ -107,15 +125,62 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 struct DevBwd {
-    int Zq, g, N, Npad, causal;
+    int Hq, g, N, Npad, causal;  // Hq: query heads per outer index; N: tokens per block
+    int ring_i0, ring_t, ring_p, bsz, n_outer;
     float scale, scale_log2;
-    const float* lse2;  // [Zq][Npad]
-    const float* dvec;  // [Zq][Npad]
-    const uint4* xl;    // [Zq][Npad]: -lse / scale as three bf16 (a 16-byte row)
-    const uint4* xd;    // [Zq][Npad]: -D as three bf16
-    uint16_t *dq, *dk, *dv;
+    const float* lse2;  // [n_z][Npad], z = query outer * Hq + head
+    const float* dvec;  // [n_z][Npad]
+    const uint4* xl;    // [n_z][Npad]: -lse / scale as three bf16 (a 16-byte row)
+    const uint4* xd;    // [n_z][Npad]: -D as three bf16
+    uint16_t *dq, *dk, *dv;  // bf16 results, or
+    float *dq_f, *dk_f, *dv_f;  // float32 results (non-null), added to when acc != 0
+    int acc;
+    int64_t q_s_head, q_s_tok, q_s_outer;  // dq strides (elements)
+    int64_t k_s_head, k_s_tok, k_s_outer;  // dk, dv strides
     int* status;
 };
+
+// Outer index o of a launch -> query outer (rank i, batch b) and KV outer
+// (rank j = (i - t) mod P, same b); the Ulysses path has one outer index, 0.
+__device__ __forceinline__ void bwd_outer(const DevBwd& p, int o, int& q_outer, int& kv_outer) {
+    const int i = p.ring_i0 + o / p.bsz, b = o % p.bsz;
+    const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
+    q_outer = i * p.bsz + b;
+    kv_outer = j * p.bsz + b;
+}
+
+// 32 consecutive values of one result row, times mul: a bf16 store, or a
+// float32 store / accumulate.
+__device__ __forceinline__ void store_row32(uint16_t* o16, float* o32, int acc, int64_t off, const uint32_t (&r)[32],
+                                            float mul) {
+    if (o32) {
+        float4* dst = reinterpret_cast<float4*>(o32 + off);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float4 v = make_float4(__uint_as_float(r[4 * e]) * mul, __uint_as_float(r[4 * e + 1]) * mul,
+                                   __uint_as_float(r[4 * e + 2]) * mul, __uint_as_float(r[4 * e + 3]) * mul);
+            if (acc) {
+                const float4 a = dst[e];
+                v.x += a.x;
+                v.y += a.y;
+                v.z += a.z;
+                v.w += a.w;
+            }
+            dst[e] = v;
+        }
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(o16 + off);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
+            v.y = pack_bf16(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
+            v.z = pack_bf16(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
+            v.w = pack_bf16(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
+            dst[e] = v;
+        }
+    }
+}
 
 // ------------------------------------------------------------------ pass 2: dK, dV
 // One 128-key tile per CTA, walked over 128-row query steps, so that every
@@ -180,9 +245,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               kPReady = kSFull + 2, kDSReady = kSFull + 3, kOReady = kSFull + 4;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int Zk = p.Zq / p.g;
-    const int kt = blockIdx.x / Zk;  // low key tiles carry the most causal work: they go first
-    const int zk = blockIdx.x % Zk;
+    const int Hkv = p.Hq / p.g;
+    const int per_kt = p.n_outer * Hkv;
+    const int kt = blockIdx.x / per_kt;  // low key tiles carry the most causal work: they go first
+    const int hk = (blockIdx.x % per_kt) % Hkv;
+    int q_outer, kv_outer;
+    bwd_outer(p, (blockIdx.x % per_kt) / Hkv, q_outer, kv_outer);
     const int n_qt = (p.N + C::kBQ - 1) / C::kBQ;
     const int qt_lo = p.causal ? kt : 0;  // kBQ == kBK: query steps before the diagonal see none of these keys
     const int nq = n_qt - qt_lo;
@@ -225,24 +293,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tma_prefetch_desc(&tm_v);
         mbar_arrive_expect_tx(BAR(kKvFull), 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_4d(sbase + C::kOffK + c * 16384, &tm_k, c * 64, zk, kt * C::kBK, 0, BAR(kKvFull));
-            tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, zk, kt * C::kBK, 0, BAR(kKvFull));
+            tma_load_4d(sbase + C::kOffK + c * 16384, &tm_k, c * 64, hk, kt * C::kBK, kv_outer, BAR(kKvFull));
+            tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, hk, kt * C::kBK, kv_outer, BAR(kKvFull));
         }
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::kStages;
-            const int zq = zk * p.g + it / nq;
+            const int hq = hk * p.g + it / nq;
             const int qt = qt_lo + it % nq;
             if (it >= C::kStages &&
                 !mbar_wait(BAR(kQEmpty + s), ((it / C::kStages) - 1) & 1, abort_p, 21, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kQFull + s), 2 * C::kTile + 2 * C::kXBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, zq, qt * C::kBQ, 0,
+                tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, hq, qt * C::kBQ, q_outer,
                             BAR(kQFull + s));
-                tma_load_4d(sbase + C::kOffDO + s * C::kTile + c * 16384, &tm_do, c * 64, zq, qt * C::kBQ, 0,
+                tma_load_4d(sbase + C::kOffDO + s * C::kTile + c * 16384, &tm_do, c * 64, hq, qt * C::kBQ, q_outer,
                             BAR(kQFull + s));
             }
-            const int64_t voff = (int64_t)zq * p.Npad + (int64_t)qt * C::kBQ;
+            const int64_t voff = ((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ;
             bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes, p.xl + voff, C::kXBytes, BAR(kQFull + s));
             bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes + C::kXBytes, p.xd + voff, C::kXBytes, BAR(kQFull + s));
         }
@@ -371,10 +439,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             // warps 0-3 write dV, warps 4-7 write dK (scale applied here)
             tc_fence_after();
             const bool valid = key < p.N;
-            const int64_t base = ((int64_t)zk * p.N + key) * D;
+            const int64_t base = (int64_t)kv_outer * p.k_s_outer + (int64_t)hk * p.k_s_head + (int64_t)key * p.k_s_tok;
             const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
             const float mul = half == 0 ? 1.f : p.scale;
-            uint16_t* out = half == 0 ? p.dv : p.dk;
+            uint16_t* out16 = half == 0 ? p.dv : p.dk;
+            float* out32 = half == 0 ? p.dv_f : p.dk_f;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t r[32];
@@ -385,18 +454,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = 0u;
                 }
-                if (valid) {
-                    uint4* dstp = reinterpret_cast<uint4*>(out + base + cc * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
-                        v.y = pack_bf16(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
-                        v.z = pack_bf16(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
-                        v.w = pack_bf16(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
-                        dstp[e] = v;
-                    }
-                }
+                if (valid) store_row32(out16, out32, p.acc, base + cc * 32, r, mul);
             }
         }
     }
@@ -455,9 +513,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int n_qt = (p.N + C::kBM - 1) / C::kBM;
-    const int qt = n_qt - 1 - (int)(blockIdx.x / p.Zq);  // heaviest query tiles first
-    const int zq = blockIdx.x % p.Zq;
-    const int zk = zq / p.g;
+    const int per_qt = p.n_outer * p.Hq;
+    const int qt = n_qt - 1 - (int)(blockIdx.x / per_qt);  // heaviest query tiles first
+    const int hq = (blockIdx.x % per_qt) % p.Hq;
+    const int hk = hq / p.g;
+    int q_outer, kv_outer;
+    bwd_outer(p, (blockIdx.x % per_qt) / p.Hq, q_outer, kv_outer);
     const int kv_end = p.causal ? min(p.N, (qt + 1) * C::kBM) : p.N;
     const int n_it = (kv_end + C::kBN - 1) / C::kBN;
 
@@ -496,8 +557,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tma_prefetch_desc(&tm_v);
         mbar_arrive_expect_tx(BAR(kQFull), 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_4d(sbase + C::kOffQ + c * 16384, &tm_q, c * 64, zq, qt * C::kBM, 0, BAR(kQFull));
-            tma_load_4d(sbase + C::kOffDO + c * 16384, &tm_do, c * 64, zq, qt * C::kBM, 0, BAR(kQFull));
+            tma_load_4d(sbase + C::kOffQ + c * 16384, &tm_q, c * 64, hq, qt * C::kBM, q_outer, BAR(kQFull));
+            tma_load_4d(sbase + C::kOffDO + c * 16384, &tm_do, c * 64, hq, qt * C::kBM, q_outer, BAR(kQFull));
         }
         for (int j = 0; j < n_it; ++j) {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
@@ -506,14 +567,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 break;
             mbar_arrive_expect_tx(BAR(kKFull + ks), C::kTile);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sbase + C::kOffK + ks * C::kTile + c * 16384, &tm_k, c * 64, zk, j * C::kBN, 0,
+                tma_load_4d(sbase + C::kOffK + ks * C::kTile + c * 16384, &tm_k, c * 64, hk, j * C::kBN, kv_outer,
                             BAR(kKFull + ks));
             if (j >= C::kVStages &&
                 !mbar_wait(BAR(kVEmpty + vs), ((j / C::kVStages) - 1) & 1, abort_p, 38, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kVFull + vs), C::kTile);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sbase + C::kOffV + vs * C::kTile + c * 16384, &tm_v, c * 64, zk, j * C::kBN, 0,
+                tma_load_4d(sbase + C::kOffV + vs * C::kTile + c * 16384, &tm_v, c * 64, hk, j * C::kBN, kv_outer,
                             BAR(kVFull + vs));
         }
     } else if (n_it > 0 && warp == kDqMmaWarp && lane == 0) {
@@ -565,7 +626,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int r = quad * 32 + lane;  // query row within the tile = TMEM lane
         const int q = qt * C::kBM + r;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const int64_t vrow = (int64_t)zq * p.Npad + q;  // q < Npad always
+        const int64_t vrow = ((int64_t)q_outer * p.Hq + hq) * p.Npad + q;  // q < Npad always
         const float lse2_r = p.lse2[vrow];
         const float dv_r = p.dvec[vrow];
         bool ok = true;
@@ -611,7 +672,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             // each warp writes half of the row's dQ columns
             tc_fence_after();
             const bool valid = q < p.N;
-            const int64_t base = ((int64_t)zq * p.N + q) * D + half * (D / 2);
+            const int64_t base =
+                (int64_t)q_outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)q * p.q_s_tok + half * (D / 2);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t rr[32];
@@ -622,18 +684,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) rr[e] = 0u;
                 }
-                if (valid) {
-                    uint4* dstp = reinterpret_cast<uint4*>(p.dq + base + cc * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(rr[8 * e + 0]) * p.scale, __uint_as_float(rr[8 * e + 1]) * p.scale);
-                        v.y = pack_bf16(__uint_as_float(rr[8 * e + 2]) * p.scale, __uint_as_float(rr[8 * e + 3]) * p.scale);
-                        v.z = pack_bf16(__uint_as_float(rr[8 * e + 4]) * p.scale, __uint_as_float(rr[8 * e + 5]) * p.scale);
-                        v.w = pack_bf16(__uint_as_float(rr[8 * e + 6]) * p.scale, __uint_as_float(rr[8 * e + 7]) * p.scale);
-                        dstp[e] = v;
-                    }
-                }
+                if (valid) store_row32(p.dq, p.dq_f, p.acc, base + cc * 32, rr, p.scale);
             }
         }
     }
@@ -652,33 +703,45 @@ struct BwdMaps {
 
 template <int D>
 bool make_bwd_maps(const BwdParams& b, int q_rows, BwdMaps* m) {
-    const int Zk = b.Zq / b.g;
-    const int64_t nd = (int64_t)b.N * D;
-    Tensor4 tq{const_cast<void*>(b.q), nd, D, nd * b.Zq, b.Zq, b.N, 1};
-    Tensor4 tdo{const_cast<void*>(b.dout), nd, D, nd * b.Zq, b.Zq, b.N, 1};
-    Tensor4 tk{const_cast<void*>(b.k), nd, D, nd * Zk, Zk, b.N, 1};
-    Tensor4 tv{const_cast<void*>(b.v), nd, D, nd * Zk, Zk, b.N, 1};
-    return make_tmap_bf16(&m->q, tq, D, q_rows) && make_tmap_bf16(&m->dout, tdo, D, q_rows) &&
-           make_tmap_bf16(&m->k, tk, D, 128) && make_tmap_bf16(&m->v, tv, D, 128);
+    return make_tmap_bf16(&m->q, b.q, D, q_rows) && make_tmap_bf16(&m->dout, b.dout, D, q_rows) &&
+           make_tmap_bf16(&m->k, b.k, D, 128) && make_tmap_bf16(&m->v, b.v, D, 128);
 }
 
+int npad_of(const BwdParams& b) { return (b.q.n_tok + 127) / 128 * 128; }
+
 DevBwd dev_params(const BwdParams& b) {
-    const int Npad = (b.N + 127) / 128 * 128;
+    const int Npad = npad_of(b);
+    const size_t rows = (size_t)b.n_z * Npad;
     DevBwd p;
-    p.Zq = b.Zq;
+    p.Hq = b.q.n_head;
     p.g = b.g;
-    p.N = b.N;
+    p.N = b.q.n_tok;
     p.Npad = Npad;
     p.causal = b.causal;
+    p.ring_i0 = b.ring_i0;
+    p.ring_t = b.ring_t;
+    p.ring_p = b.ring_p;
+    p.bsz = b.bsz;
+    p.n_outer = b.n_outer;
     p.scale = b.scale;
     p.scale_log2 = b.scale * kLog2e;
-    p.dvec = b.dvec;
-    p.lse2 = b.dvec + (size_t)b.Zq * Npad;
-    p.xl = reinterpret_cast<const uint4*>(b.dvec + 2 * (size_t)b.Zq * Npad);
-    p.xd = p.xl + (size_t)b.Zq * Npad;
+    p.dvec = b.ws;
+    p.lse2 = b.ws + rows;
+    p.xl = reinterpret_cast<const uint4*>(b.ws + 2 * rows);
+    p.xd = p.xl + rows;
     p.dq = static_cast<uint16_t*>(b.dq);
     p.dk = static_cast<uint16_t*>(b.dk);
     p.dv = static_cast<uint16_t*>(b.dv);
+    p.dq_f = b.dq_f32;
+    p.dk_f = b.dk_f32;
+    p.dv_f = b.dv_f32;
+    p.acc = b.accumulate;
+    p.q_s_head = b.q.s_head;
+    p.q_s_tok = b.q.s_tok;
+    p.q_s_outer = b.q.s_outer;
+    p.k_s_head = b.k.s_head;
+    p.k_s_tok = b.k.s_tok;
+    p.k_s_outer = b.k.s_outer;
     p.status = b.status;
     return p;
 }
@@ -686,10 +749,28 @@ DevBwd dev_params(const BwdParams& b) {
 template <int D>
 cudaError_t pre_t(const BwdParams& b, cudaStream_t stream) {
     const DevBwd p = dev_params(b);
-    const int64_t rows = (int64_t)b.Zq * p.Npad;
-    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(b.o), static_cast<const uint16_t*>(b.dout), b.lse, const_cast<float*>(p.dvec),
-        const_cast<float*>(p.lse2), const_cast<uint4*>(p.xl), const_cast<uint4*>(p.xd), b.scale, b.Zq, b.N, p.Npad);
+    PreArgs a;
+    a.o = static_cast<const uint16_t*>(b.o.ptr);
+    a.dout = static_cast<const uint16_t*>(b.dout.ptr);
+    a.lse = b.lse;
+    a.s_head = b.o.s_head;
+    a.s_tok = b.o.s_tok;
+    a.s_outer = b.o.s_outer;
+    a.l_s_head = b.l_s_head;
+    a.l_s_tok = b.l_s_tok;
+    a.l_s_outer = b.l_s_outer;
+    a.heads = b.q.n_head;
+    a.N = b.q.n_tok;
+    a.Npad = p.Npad;
+    a.n_z = b.n_z;
+    a.scale = b.scale;
+    a.dvec = const_cast<float*>(p.dvec);
+    a.lse2 = const_cast<float*>(p.lse2);
+    a.xl = const_cast<uint4*>(p.xl);
+    a.xd = const_cast<uint4*>(p.xd);
+    const int64_t rows = (int64_t)b.n_z * p.Npad;
+    if (rows == 0) return cudaSuccess;
+    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -700,9 +781,10 @@ cudaError_t dkdv_t(const BwdParams& b, cudaStream_t stream) {
     auto kern = dkdv_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int n_kt = (b.N + 127) / 128;
-    kern<<<(unsigned)(n_kt * (b.Zq / b.g)), kKvThreads, KvCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v,
-                                                                                      dev_params(b));
+    const int64_t n_kt = (b.q.n_tok + 127) / 128;
+    const int64_t grid = n_kt * b.n_outer * (b.q.n_head / b.g);
+    if (grid == 0) return cudaSuccess;
+    kern<<<(unsigned)grid, kKvThreads, KvCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
     return cudaGetLastError();
 }
 
@@ -713,8 +795,10 @@ cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
     auto kern = dq_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int n_qt = (b.N + 127) / 128;
-    kern<<<(unsigned)(n_qt * b.Zq), kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
+    const int64_t n_qt = (b.q.n_tok + 127) / 128;
+    const int64_t grid = n_qt * b.n_outer * b.q.n_head;
+    if (grid == 0) return cudaSuccess;
+    kern<<<(unsigned)grid, kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
     return cudaGetLastError();
 }
 

@@ -56,20 +56,32 @@ struct FwdParams {
 };
 cudaError_t launch_attn_fwd_bf16(const FwdParams& p, cudaStream_t stream);
 
-// Backward (head-sharded).  q, o, dout, dq: [Zq][N][d]; k, v, dk, dv: [Zq/g][N][d];
-// lse, dvec: [Zq][N] float32.
+// Backward.  Tensors are addressed as (d, head, token, outer) like the
+// forward: the Ulysses path passes head-sharded buffers as B*Hq "heads" of N
+// tokens with one outer index; ring mode passes sequence-sharded buffers
+// ([P][B][N/P][H][d], outer = rank * B + b) and one launch per ring step, the
+// launch's outer indices decoded as in FwdParams (query outer i*bsz + b, KV
+// outer j*bsz + b with j = (i - ring_t) mod ring_p).
 struct BwdParams {
-    const void *q, *k, *v, *o, *dout;
-    const float* lse;
-    float* dvec;  // workspace base: D_i = dO_i . O_i, then lse_i*log2(e), [Zq][Npad] each (float32),
-                  // then -lse_i/scale and -D_i as 16-byte rows of three bf16, [Zq][Npad] each
+    Tensor4 q, k, v, o, dout;  // o and dout shaped and strided as q
+    const float* lse;          // strides l_s_*: element of (head, token, outer)
+    int64_t l_s_head, l_s_tok, l_s_outer;
+    float* ws;  // workspace base: per query row z*Npad + n (z = outer * heads + head), padded to 128:
+                // D_i = dO_i . O_i and lse_i*log2(e) (float32), then -lse_i/scale and -D_i as
+                // 16-byte rows of three bf16
+    int n_z;    // query (outer, head) pairs covered by the workspace
+    // results: bf16 (dq strided as q, dk and dv as k), or float32 arrays with the
+    // same strides, overwritten or (accumulate != 0) added to
     void *dq, *dk, *dv;
-    int Zq, g, N, d, causal;
+    float *dq_f32, *dk_f32, *dv_f32;
+    int accumulate;
+    int d, g, causal;
+    int ring_i0, ring_t, ring_p, bsz, n_outer;  // Ulysses: 0, 0, 1, 1, 1
     float scale;
     int* status;
 };
-// The three passes, in this order: D_i and lse_i*log2(e) into the workspace
-// (rows padded to 128), then dK/dV, then dQ.  p.dvec is the workspace base.
+// The three passes, in this order: the workspace rows (launch_bwd_pre covers
+// all n_z rows), then dK/dV, then dQ (these two cover the launch's outer indices).
 cudaError_t launch_bwd_pre(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream);

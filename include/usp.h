@@ -183,6 +183,33 @@ size_t usp_ring_workspace_size(const usp_problem* p);
 usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
                              float* lse, void* ws, size_t ws_bytes, usp_stream stream);
 
+/* Bytes of workspace usp_ring_attn_bwd needs: 40 bytes per query row of
+ * every rank and head (rows padded to 128 per rank: D_i and lse_i*log2(e) as
+ * float32, -lse_i/scale and -D_i as three bf16 each), plus float32
+ * accumulators for dQ, dK and dV (d values per row) -- linear in N. */
+size_t usp_ring_bwd_workspace_size(const usp_problem* p);
+
+/* Ring attention backward on sequence-sharded buffers: the gradients of the
+ * causal attention of the whole sequence, computed with the ring schedule of
+ * usp_ring_attn_fwd ("Context Parallelism", ultralytics.com, "So funktioniert
+ * Kontextparallelitaet": at step t = 0..P-1 rank i holds KV block
+ * j = (i - t) mod P, skipped when j > i under the causal mask, masked only
+ * when j == i).  Each step adds rank i's partial gradients for the block
+ * pair (i, j), taken with the merged LSE of the forward and D_i = dO_i . O_i:
+ *   dQ_i += scale sum_j dS_ij K_j   (stays on rank i)
+ *   dK_j += scale sum_{h in group} sum_i dS_ij Q_i,  dV_j += sum P_ij dO_i
+ *                                   (travel with the KV block)
+ * in float32, then rounds once to bf16.  The pages name no ring backward;
+ * this is the plain reading that the forward's schedule and the backward of
+ * the glossary page's example leave.
+ * q, o, dout, dq: [P][B][N/P][Hq][d] bf16; k, v, dk, dv: [P][B][N/P][Hkv][d]
+ * bf16; lse: float32 [P][B][N/P][Hq] from usp_ring_attn_fwd.  ws: at least
+ * usp_ring_bwd_workspace_size(p) bytes, 256-byte aligned, contents on entry
+ * irrelevant.  dtype BF16, d in {64, 128}; Hq % Hkv == 0; N % P == 0. */
+usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                             size_t ws_bytes, usp_stream stream);
+
 /* Exact merge of two partial attentions over disjoint key sets, float32
  * (the merge step of ring attention):
  *   lse = ln(exp(lse_a) + exp(lse_b))

@@ -108,6 +108,22 @@ def test_backward_and_ring_argument_errors(lib):
     with pytest.raises(usp.UspError) as e:
         usp.usp_ring_merge(10, 6, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)   # d % 4
     assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    bws = usp.usp_ring_bwd_workspace_size(p)
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_ring_attn_bwd(p, *([FAKE] * 9), FAKE, bws - 256)
+    assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_ring_attn_bwd(p, *([FAKE] * 9), FAKE + 128, bws)   # workspace must be 256-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_ring_attn_bwd(p, FAKE + 8, *([FAKE] * 8), FAKE, bws)   # q not 16-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_ring_attn_bwd(_p(d=96), *([FAKE] * 9), FAKE, bws)
+    assert e.value.status == _lib.USP_ERR_UNSUPPORTED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_ring_attn_bwd(_p(dtype="f32"), *([FAKE] * 9), FAKE, bws)
+    assert e.value.status == _lib.USP_ERR_UNSUPPORTED
 
 
 def test_empty_problems_enqueue_nothing(lib):
@@ -118,6 +134,7 @@ def test_empty_problems_enqueue_nothing(lib):
         usp.usp_attn_fwd(p, 0, 0, 0, 0, 0)
         usp.usp_attn_bwd(p, *([0] * 9), 0, 0)
         usp.usp_ring_attn_fwd(p, 0, 0, 0, 0, 0, 0, 0)
+        usp.usp_ring_attn_bwd(p, *([0] * 9), 0, 0)
     usp.usp_ring_merge(0, 64, 0, 0, 0, 0, 0, 0)
 
 
@@ -130,6 +147,11 @@ def test_workspaces_are_linear_in_sequence_length(lib):
         r1 = usp.usp_ring_workspace_size(_p(N=N, Hq=32, Hkv=32, d=128, P=8))
         r2 = usp.usp_ring_workspace_size(_p(N=2 * N, Hq=32, Hkv=32, d=128, P=8))
         assert r2 == 2 * r1
+        b1 = usp.usp_ring_bwd_workspace_size(_p(N=N, Hq=32, Hkv=8, d=128, P=8))
+        b2 = usp.usp_ring_bwd_workspace_size(_p(N=2 * N, Hq=32, Hkv=8, d=128, P=8))
+        assert b2 == 2 * b1
+        # 40 bytes per padded query row, float32 dQ (Hq) and dK, dV (Hkv) accumulators
+        assert b1 == 40 * 32 * N + 4 * N * 128 * (32 + 2 * 8)
     assert usp.usp_attn_bwd_workspace_size(_p(N=255)) == 0  # invalid problem
 
 
