@@ -447,7 +447,7 @@ def run_usp(args, world, rank, local):
 
 
 def bench_ring(usp, torch, dev, peaks):
-    """Ring attention forward on the 512K-token workload (one timed call)."""
+    """Ring attention forward and backward on the 512K-token workload (one timed call each)."""
     import numpy as np
     import synth
     w = RING
@@ -479,12 +479,35 @@ def bench_ring(usp, torch, dev, peaks):
     ms = e0.elapsed_time(e1)
     f = fwd_flops(w)
     ok = usp.usp_device_status(s.cuda_stream) == 0
-    del q, k, v, o, lse, ws
+    del ws
     torch.cuda.empty_cache()
-    return {"workload": "512K-token ring attention forward, B=1, H=32, d=128, P=8 (shards of 65536)",
+
+    # backward with a seeded upstream gradient: one untimed call, then one timed call
+    dout = upload(p.seq_shape(w["Hq"]), synth.STREAM_DO)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(usp.usp_ring_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    usp.usp_ring_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, bws, None, s.cuda_stream)
+    torch.cuda.synchronize()
+    usp.usp_trace_reset()
+    usp.usp_trace_enable(True)
+    e0.record(s)
+    usp.usp_ring_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, bws, None, s.cuda_stream)
+    e1.record(s)
+    torch.cuda.synchronize()
+    usp.usp_trace_enable(False)
+    btrace = usp.usp_trace_report()
+    bms = e0.elapsed_time(e1)
+    bf = 2.5 * f  # backward: 10*d FLOPs per visible pair against the forward's 4*d
+    ok = ok and usp.usp_device_status(s.cuda_stream) == 0
+    del q, k, v, o, lse, dout, dq, dk, dv, bws
+    torch.cuda.empty_cache()
+    return {"workload": "512K-token ring attention forward and backward, B=1, H=32, d=128, P=8 (shards of 65536)",
             "ms": ms, "TFLOPs": f / (ms * 1e-3) / 1e12, "frac_sustained": f / (ms * 1e-3) / 1e12 / peaks["bf16_sus"],
-            "kernels_ms": {k_: v_[1] for k_, v_ in trace.items()}, "status_ok": ok,
-            "data": "seeded Philox N(0,1) bf16 (seed 0, streams Q/K/V), sequence-sharded"}
+            "kernels_ms": {k_: v_[1] for k_, v_ in trace.items()},
+            "bwd_ms": bms, "bwd_TFLOPs": bf / (bms * 1e-3) / 1e12,
+            "bwd_frac_sustained": bf / (bms * 1e-3) / 1e12 / peaks["bf16_sus"],
+            "bwd_kernels_ms": {k_: v_[1] for k_, v_ in btrace.items()}, "status_ok": ok,
+            "data": "seeded Philox N(0,1) bf16 (seed 0, streams Q/K/V/dO), sequence-sharded"}
 
 
 def main():

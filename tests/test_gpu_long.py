@@ -7,7 +7,9 @@ oracle cannot afford every row) and against properties that hold at any size:
     (their rows i >= j are few enough for the oracle), plus
     sum_j dK_j = 0 (softmax shift invariance) and sum_j dV_j = sum_i dO_i,
     within the bound the per-element tolerance implies for a sum;
-  - ring attention equals one full-sequence pass and the oracle's rows.
+  - ring attention equals one full-sequence pass and the oracle's rows;
+  - ring backward gradients against the oracle on sampled dQ rows and tail
+    dK/dV rows, plus the same sum identities.
 """
 import os
 
@@ -85,6 +87,14 @@ def test_ulysses_long_context(usp, orc, B, Hq, Hkv, N, d, P):
     assert rel_fro(f64(o[:, :, rows]), o_ref) < TOL_BF16_O_RELFRO
     assert max_abs(lse[:, :, rows], lse_ref) < TOL_LSE_BF16
 
+    _check_sampled_grads(q, k, v, dO, dq, dk, dv, P)
+
+
+def _check_sampled_grads(q, k, v, dO, dq, dk, dv, P):
+    """dQ on seeded rows, dK/dV on the last key rows, and the sum identities."""
+    from oracle import rows_blas
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
     # dQ on sampled rows
     rq = sample_rows(N, DQ_ROWS, P, seed=2)
     dq_ref = rows_blas.attn_bwd_q_rows(q, k, v, dO, rq, causal=True)
@@ -115,7 +125,7 @@ def test_ulysses_long_context(usp, orc, B, Hq, Hkv, N, d, P):
 
 
 def test_ring_512k(usp, orc):
-    """512K tokens, 32 heads, d=128, P=8 shards of 65536: ring forward."""
+    """512K tokens, 32 heads, d=128, P=8 shards of 65536: ring forward and backward."""
     import torch
     from oracle import rows_blas
     B, H, N, d, P = 1, 32, 524288, 128, 8
@@ -132,7 +142,14 @@ def test_ring_512k(usp, orc):
     o_ring, lse_ring = usp.ring_attention_fwd(p, qs, ks, vs)
     torch.cuda.synchronize()
     assert usp.usp_device_status() == 0
-    del qs, ks, vs
+    # ring backward with a seeded upstream gradient
+    dO = gen((B, H, N, d), 3)
+    dos = _seq_on_device(to_dev(dO), P)
+    dq_s, dk_s, dv_s = usp.ring_attention_bwd(p, qs, ks, vs, o_ring, lse_ring, dos)
+    torch.cuda.synchronize()
+    assert usp.usp_device_status() == 0
+    dq, dk, dv = (to_host(_logical_from_seq(x)) for x in (dq_s, dk_s, dv_s))
+    del qs, ks, vs, dos, dq_s, dk_s, dv_s
     o_ring_l = _logical_from_seq(o_ring)
     lse_ring_l = lse_ring.permute(1, 3, 0, 2).reshape(B, H, N)
     # ring == one pass (both bf16 outputs of float32 arithmetic)
@@ -149,3 +166,4 @@ def test_ring_512k(usp, orc):
     assert max_abs(f64(o[:, :, rows]), o_ref) < TOL_BF16_O_MAXABS
     assert rel_fro(f64(o[:, :, rows]), o_ref) < TOL_BF16_O_RELFRO
     assert max_abs(lse[:, :, rows], lse_ref) < TOL_LSE_BF16
+    _check_sampled_grads(q, k, v, dO, dq, dk, dv, P)
