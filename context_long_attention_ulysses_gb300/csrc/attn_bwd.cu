@@ -401,14 +401,18 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const int qmin_ok = key - q0;  // columns e with q0 + e >= key are visible
             float pf[64];
             uint32_t pk[32];
+            const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const float sv = __uint_as_float(e + u < 32 ? ra[e + u] : rb[e + u - 32]);
-                    float pv = ex2_approx(sv * p.scale_log2);  // S' already holds S - lse / scale
-                    if (need_mask && e + u < qmin_ok) pv = 0.f;
-                    pf[e + u] = pv;
+                // S' already holds S - lse / scale: P = 2^(S' scale log2 e), column pairs in packed float32
+                const float2 x = mul2(make_float2(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]),
+                                                  __uint_as_float(e < 32 ? ra[e + 1] : rb[e - 31])),
+                                      c2);
+                pf[e] = ex2_approx(x.x);
+                pf[e + 1] = ex2_approx(x.y);
+                if (need_mask) {
+                    if (e < qmin_ok) pf[e] = 0.f;
+                    if (e + 1 < qmin_ok) pf[e + 1] = 0.f;
                 }
                 pk[e / 2] = pack_bf16(pf[e], pf[e + 1]);
             }
@@ -425,9 +429,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
                 // dP' already holds dP - D
-                const float ds0 = pf[e] * __uint_as_float(e < 32 ? ra[e] : rb[e - 32]);
-                const float ds1 = pf[e + 1] * __uint_as_float(e + 1 < 32 ? ra[e + 1] : rb[e - 31]);
-                pk[e / 2] = pack_bf16(ds0, ds1);
+                const float2 ds = mul2(make_float2(pf[e], pf[e + 1]),
+                                       make_float2(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]),
+                                                   __uint_as_float(e < 32 ? ra[e + 1] : rb[e - 31])));
+                pk[e / 2] = pack_bf16(ds.x, ds.y);
             }
             tmem_st32(lane_base + col_dp, pk);  // dS^T over the first 32 of this warp's dP^T columns
             tmem_wait_st();
@@ -647,19 +652,23 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc_fence_before();
             mbar_arrive(BAR(kSFree));  // S and dP of step j are in registers: the next products may start
             uint32_t dsp[32];
+            const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nl2 = make_float2(-lse2_r, -lse2_r), nd2 = make_float2(-dv_r, -dv_r);
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
-                const float sv0 = __uint_as_float(e < 32 ? sa[e] : sb[e - 32]);
-                const float sv1 = __uint_as_float(e < 32 ? sa[e + 1] : sb[e - 31]);
-                const float dp0 = __uint_as_float(e < 32 ? da[e] : db[e - 32]);
-                const float dp1 = __uint_as_float(e < 32 ? da[e + 1] : db[e - 31]);
-                float p0 = ex2_approx(fmaf(sv0, p.scale_log2, -lse2_r));
-                float p1 = ex2_approx(fmaf(sv1, p.scale_log2, -lse2_r));
+                // column pairs in packed float32: x = S c - lse2, P = 2^x, dS = P (dP - D)
+                const float2 sv = make_float2(__uint_as_float(e < 32 ? sa[e] : sb[e - 32]),
+                                              __uint_as_float(e < 32 ? sa[e + 1] : sb[e - 31]));
+                const float2 dp = make_float2(__uint_as_float(e < 32 ? da[e] : db[e - 32]),
+                                              __uint_as_float(e < 32 ? da[e + 1] : db[e - 31]));
+                const float2 x = fma2(sv, c2, nl2);
+                float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                 if (need_mask) {
-                    if (e > climit) p0 = 0.f;
-                    if (e + 1 > climit) p1 = 0.f;
+                    if (e > climit) pv.x = 0.f;
+                    if (e + 1 > climit) pv.y = 0.f;
                 }
-                dsp[e / 2] = pack_bf16(p0 * (dp0 - dv_r), p1 * (dp1 - dv_r));
+                const float2 ds = mul2(pv, add2(dp, nd2));
+                dsp[e / 2] = pack_bf16(ds.x, ds.y);
             }
             // dS (bf16) of keys 64 half .. + 63 into columns 32 half .. + 31 of this step's buffer
             tmem_st32(lane_base + ((j & 1) ? C::kColDS1 : C::kColDS0) + half * 32, dsp);

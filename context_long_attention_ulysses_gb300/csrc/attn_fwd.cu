@@ -292,14 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN; ++c)
                     if (c > climit) s[c] = -INFINITY;
             }
-            // row max as eight independent chains
+            // row max as eight independent chains of three-input maxima
             float m8[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) m8[c] = s[c];
 #pragma unroll
-            for (int c = 8; c < kBN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int c = 8; c < kBN; c += 2) m8[(c / 2) & 7] = max3f(m8[(c / 2) & 7], s[c], s[c + 1]);
+            float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             mx *= p.scale_log2;
             const float m_new = fmaxf(m_run, mx);
             const bool rescale = m_new > m_run + kRescaleThreshold;
