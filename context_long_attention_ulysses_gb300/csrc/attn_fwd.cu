@@ -311,8 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * c], p.scale_log2, -msub));
-                    const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * c + 1], p.scale_log2, -msub));
+                    const float2 x = fma2(make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]),
+                                          make_float2(p.scale_log2, p.scale_log2), make_float2(-msub, -msub));
+                    const float p0 = ex2_approx(x.x);
+                    const float p1 = ex2_approx(x.y);
                     sum4[c & 3] += p0 + p1;
                     pk[c] = pack_bf16(p0, p1);
                 }
