@@ -29,6 +29,8 @@ __all__ = [
     "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "usp_attn_bwd_noalloc",
     "NOALLOC_SCRATCH_BYTES", "ulysses_attention_fwd", "ulysses_attention_bwd", "ring_attention_fwd", "library_path",
     "usp_ring_bwd_workspace_size", "usp_ring_attn_bwd", "ring_attention_bwd",
+    "usp_allgather_workspace_size", "usp_allgather_attn_fwd", "usp_allgather_bwd_workspace_size",
+    "usp_allgather_attn_bwd", "allgather_attention_fwd", "allgather_attention_bwd",
 ]
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -170,6 +172,29 @@ def usp_ring_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, s
                                                         int(ws_bytes), _stream(stream)))
 
 
+def usp_allgather_workspace_size(p) -> int:
+    return int(load().usp_allgather_workspace_size(_prob(p)))
+
+
+def usp_allgather_attn_fwd(p, q, k, v, o, lse, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_allgather_attn_fwd", load().usp_allgather_attn_fwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                                  _ptr(lse), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def usp_allgather_bwd_workspace_size(p) -> int:
+    return int(load().usp_allgather_bwd_workspace_size(_prob(p)))
+
+
+def usp_allgather_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_allgather_attn_bwd", load().usp_allgather_attn_bwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                                  _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                                                  _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
 def usp_ring_merge(rows: int, d: int, o_a, lse_a, o_b, lse_b, o, lse, stream=None) -> None:
     check("usp_ring_merge", load().usp_ring_merge(int(rows), int(d), _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b),
                                                   _ptr(o), _ptr(lse), _stream(stream)))
@@ -263,6 +288,25 @@ def ring_attention_fwd(p: Problem, q_seq, k_seq, v_seq, stream=None):
     ws = torch.empty(max(usp_ring_workspace_size(p), 256), dtype=torch.uint8, device=dev)
     usp_ring_attn_fwd(p, q_seq, k_seq, v_seq, o, lse, ws, None, stream)
     return o, lse
+
+
+def allgather_attention_fwd(p: Problem, q_seq, k_seq, v_seq, stream=None):
+    """All-gather-KV attention forward on sequence-sharded buffers: returns (o_seq, lse_seq)."""
+    dev, dt = q_seq.device, p.torch_dtype
+    o = _empty(p.seq_shape(p.Hq), dt, dev)
+    lse = _empty(p.lse_seq_shape(), torch.float32, dev)
+    ws = torch.empty(max(usp_allgather_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    usp_allgather_attn_fwd(p, q_seq, k_seq, v_seq, o, lse, ws, None, stream)
+    return o, lse
+
+
+def allgather_attention_bwd(p: Problem, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq, stream=None):
+    """All-gather-KV attention backward on sequence-sharded buffers: returns (dq_seq, dk_seq, dv_seq)."""
+    dev = q_seq.device
+    dq, dk, dv = torch.empty_like(q_seq), torch.empty_like(k_seq), torch.empty_like(v_seq)
+    ws = torch.empty(max(usp_allgather_bwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    usp_allgather_attn_bwd(p, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq, dq, dk, dv, ws, None, stream)
+    return dq, dk, dv
 
 
 def ring_attention_bwd(p: Problem, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq, stream=None):

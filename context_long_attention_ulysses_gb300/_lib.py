@@ -29,7 +29,8 @@ SYMBOLS = (
     "usp_a2a_seq2head", "usp_a2a_head2seq", "usp_attn_fwd", "usp_attn_bwd_workspace_size", "usp_attn_bwd",
     "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
     "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "usp_attn_bwd_noalloc",
-    "usp_ring_bwd_workspace_size", "usp_ring_attn_bwd",
+    "usp_ring_bwd_workspace_size", "usp_ring_attn_bwd", "usp_allgather_workspace_size", "usp_allgather_attn_fwd",
+    "usp_allgather_bwd_workspace_size", "usp_allgather_attn_bwd",
 )
 
 
@@ -89,6 +90,10 @@ def load() -> ctypes.CDLL:
             "usp_attn_bwd_noalloc": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "usp_ring_bwd_workspace_size": (sz, [P]),
             "usp_ring_attn_bwd": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "usp_allgather_workspace_size": (sz, [P]),
+            "usp_allgather_attn_fwd": (ci, [P, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "usp_allgather_bwd_workspace_size": (sz, [P]),
+            "usp_allgather_attn_bwd": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

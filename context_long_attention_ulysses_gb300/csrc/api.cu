@@ -3,6 +3,7 @@
 // out; the library never allocates device memory.
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <map>
 #include <mutex>
 #include <string>
@@ -479,6 +480,167 @@ usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k,
     e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dq, dq, (int64_t)q_elems, s); });
     if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dk, dk, (int64_t)k_elems, s); });
     if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dv, dv, (int64_t)k_elems, s); });
+    return cuda_status(e);
+}
+
+// ---- all-gather-KV context parallelism
+// Workspace: the gathered K and V (bf16, [B][N][Hkv][d]); the backward adds
+// its 40-byte rows per padded query row of every rank and head and float32
+// dK, dV accumulators in the gathered layout.
+static size_t gathered_bytes(const usp_problem* p) { return (size_t)p->B * p->N * p->Hkv * p->d * 2; }
+
+size_t usp_allgather_workspace_size(const usp_problem* p) {
+    if (check_problem(p, false) != USP_OK) return 0;
+    return 2 * ring_part(gathered_bytes(p));
+}
+
+size_t usp_allgather_bwd_workspace_size(const usp_problem* p) {
+    if (check_problem(p, false) != USP_OK) return 0;
+    return 2 * ring_part(gathered_bytes(p)) + ring_part(ring_bwd_rows(p) * 40) + 2 * ring_part(gathered_bytes(p) * 2);
+}
+
+static usp_status allgather_checks(const usp_problem* p, std::initializer_list<const void*> ptrs, const void* ws) {
+    usp_status st = check_problem(p, false);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
+    if ((int64_t)p->B * p->P > 65535) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    return USP_OK;
+}
+
+// Every rank's K and V shard into one sequence per batch: one copy per (rank, batch) chunk.
+static cudaError_t gather_kv(const usp_problem* p, const void* k, const void* v, void* kg, void* vg, cudaStream_t s) {
+    const int P = p->P, B = p->B, Np = p->N / P;
+    const size_t row = (size_t)p->Hkv * p->d * 2, chunk = (size_t)Np * row;
+    return traced("allgather_kv", s, [&] {
+        for (int i = 0; i < P; ++i)
+            for (int b = 0; b < B; ++b) {
+                const size_t src = ((size_t)i * B + b) * chunk, dst = ((size_t)b * p->N + (size_t)i * Np) * row;
+                cudaError_t e = cudaMemcpyAsync(static_cast<char*>(kg) + dst, static_cast<const char*>(k) + src, chunk,
+                                                cudaMemcpyDeviceToDevice, s);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(static_cast<char*>(vg) + dst, static_cast<const char*>(v) + src, chunk,
+                                        cudaMemcpyDeviceToDevice, s);
+                if (e != cudaSuccess) return e;
+            }
+        return cudaSuccess;
+    });
+}
+
+usp_status usp_allgather_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
+                                  float* lse, void* ws, size_t ws_bytes, usp_stream stream) {
+    usp_status st = allgather_checks(p, {q, k, v, o, lse}, ws);
+    if (st != USP_OK || empty(p)) return st;
+    if (ws_bytes < usp_allgather_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d, N = p->N, Np = N / P;
+    void* kg = ws;
+    void* vg = static_cast<char*>(ws) + ring_part(gathered_bytes(p));
+    if (gather_kv(p, k, v, kg, vg, s) != cudaSuccess) return USP_ERR_CUDA;
+
+    FwdParams f{};
+    f.q = Tensor4{const_cast<void*>(q), d, (int64_t)Hq * d, (int64_t)Np * Hq * d, Hq, Np, P * B};
+    f.k = Tensor4{kg, d, (int64_t)Hkv * d, (int64_t)N * Hkv * d, Hkv, N, B};
+    f.v = Tensor4{vg, d, (int64_t)Hkv * d, (int64_t)N * Hkv * d, Hkv, N, B};
+    f.d = d;
+    f.g = Hq / Hkv;
+    f.n_heads = Hq;
+    f.n_outer = P * B;
+    f.q_len = Np;
+    f.kv_len = N;
+    f.ring_i0 = 0;
+    f.ring_t = 0;
+    f.ring_p = P;
+    f.bsz = B;
+    f.np = Np;
+    f.kv_gathered = 1;
+    f.causal = p->causal ? 1 : 0;
+    f.scale = eff_scale(p);
+    f.o_bf16 = o;
+    f.o_s_head = d;
+    f.o_s_tok = (int64_t)Hq * d;
+    f.o_s_outer = (int64_t)Np * Hq * d;
+    f.lse = lse;
+    f.l_s_head = 1;
+    f.l_s_tok = Hq;
+    f.l_s_outer = (int64_t)Np * Hq;
+    f.status = sp;
+    return cuda_status(traced("allgather_attn_fwd", s, [&] { return launch_attn_fwd_bf16(f, s); }));
+}
+
+usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                                  size_t ws_bytes, usp_stream stream) {
+    usp_status st = allgather_checks(p, {q, k, v, o, lse, dout, dq, dk, dv}, ws);
+    if (st != USP_OK || empty(p)) return st;
+    if (ws_bytes < usp_allgather_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d, N = p->N, Np = N / P;
+    char* w = static_cast<char*>(ws);
+    void* kg = w;
+    void* vg = w + ring_part(gathered_bytes(p));
+    float* rows = reinterpret_cast<float*>(w + 2 * ring_part(gathered_bytes(p)));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(rows) + ring_part(ring_bwd_rows(p) * 40));
+    float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(gathered_bytes(p) * 2));
+    if (gather_kv(p, k, v, kg, vg, s) != cudaSuccess) return USP_ERR_CUDA;
+
+    BwdParams b{};
+    const int64_t qs_tok = (int64_t)Hq * d, ks_tok = (int64_t)Hkv * d;
+    b.q = Tensor4{const_cast<void*>(q), d, qs_tok, (int64_t)Np * qs_tok, Hq, Np, P * B};
+    b.o = Tensor4{const_cast<void*>(o), d, qs_tok, (int64_t)Np * qs_tok, Hq, Np, P * B};
+    b.dout = Tensor4{const_cast<void*>(dout), d, qs_tok, (int64_t)Np * qs_tok, Hq, Np, P * B};
+    b.k = Tensor4{kg, d, ks_tok, (int64_t)N * ks_tok, Hkv, N, B};
+    b.v = Tensor4{vg, d, ks_tok, (int64_t)N * ks_tok, Hkv, N, B};
+    b.lse = lse;
+    b.l_s_head = 1;
+    b.l_s_tok = Hq;
+    b.l_s_outer = (int64_t)Np * Hq;
+    b.ws = rows;
+    b.n_z = P * B * Hq;
+    b.dq = dq;  // dQ_i is complete after one pass of rank i over the gathered keys: bf16 directly
+    b.dk_f32 = acc_dk;
+    b.dv_f32 = acc_dv;
+    b.d = d;
+    b.g = Hq / Hkv;
+    b.causal = p->causal ? 1 : 0;
+    b.ring_t = 0;
+    b.ring_p = P;
+    b.bsz = B;
+    b.kv_gathered = 1;
+    b.scale = eff_scale(p);
+    b.status = sp;
+
+    cudaError_t e = traced("allgather_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
+    b.ring_i0 = 0;
+    b.n_outer = P * B;
+    if (e == cudaSuccess) e = traced("allgather_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
+    // dK, dV: rank i's partial over the gathered keys, summed over the ranks in float32 (the
+    // reduce part of a reduce-scatter), one launch per rank in rank order
+    for (int i = 0; e == cudaSuccess && i < P; ++i) {
+        b.ring_i0 = i;
+        b.n_outer = B;
+        b.accumulate = i > 0 ? 1 : 0;
+        e = traced("allgather_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+    }
+    // the scatter part: rank j keeps the rows of its own shard, rounded to bf16
+    const int64_t chunk = (int64_t)Np * Hkv * d;
+    for (int j = 0; e == cudaSuccess && j < P; ++j)
+        for (int bb = 0; e == cudaSuccess && bb < B; ++bb) {
+            const int64_t src = ((int64_t)bb * N + (int64_t)j * Np) * Hkv * d, dst = ((int64_t)j * B + bb) * chunk;
+            e = traced("allgather_scatter", s, [&] {
+                cudaError_t e2 = launch_f32_to_bf16(acc_dk + src, static_cast<uint16_t*>(dk) + dst, chunk, s);
+                return e2 == cudaSuccess ? launch_f32_to_bf16(acc_dv + src, static_cast<uint16_t*>(dv) + dst, chunk, s)
+                                         : e2;
+            });
+        }
     return cuda_status(e);
 }
 

@@ -125,8 +125,9 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 struct DevBwd {
-    int Hq, g, N, Npad, causal;  // Hq: query heads per outer index; N: tokens per block
-    int ring_i0, ring_t, ring_p, bsz, n_outer;
+    int Hq, g, N, Npad, causal;  // Hq: query heads per outer index; N: query tokens per block
+    int Nkv;                     // key tokens per block
+    int ring_i0, ring_t, ring_p, bsz, n_outer, kv_gathered;
     float scale, scale_log2;
     const float* lse2;  // [n_z][Npad], z = query outer * Hq + head
     const float* dvec;  // [n_z][Npad]
@@ -140,13 +141,17 @@ struct DevBwd {
     int* status;
 };
 
-// Outer index o of a launch -> query outer (rank i, batch b) and KV outer
-// (rank j = (i - t) mod P, same b); the Ulysses path has one outer index, 0.
-__device__ __forceinline__ void bwd_outer(const DevBwd& p, int o, int& q_outer, int& kv_outer) {
+// Outer index o of a launch -> query outer (rank i, batch b), KV outer (rank
+// j = (i - t) mod P and batch b; batch b alone when K/V are gathered) and the
+// causal shift: the position of the query block's first token minus that of
+// the key block's (query q sees key k, both block-local, iff q + shift >= k).
+// The Ulysses path has one outer index, 0, and shift 0.
+__device__ __forceinline__ void bwd_outer(const DevBwd& p, int o, int& q_outer, int& kv_outer, int& shift) {
     const int i = p.ring_i0 + o / p.bsz, b = o % p.bsz;
     const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
     q_outer = i * p.bsz + b;
-    kv_outer = j * p.bsz + b;
+    kv_outer = p.kv_gathered ? b : j * p.bsz + b;
+    shift = p.kv_gathered ? i * p.N : (i - j) * p.N;
 }
 
 // 32 consecutive values of one result row, times mul: a bf16 store, or a
@@ -249,11 +254,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int per_kt = p.n_outer * Hkv;
     const int kt = blockIdx.x / per_kt;  // low key tiles carry the most causal work: they go first
     const int hk = (blockIdx.x % per_kt) % Hkv;
-    int q_outer, kv_outer;
-    bwd_outer(p, (blockIdx.x % per_kt) / Hkv, q_outer, kv_outer);
+    int q_outer, kv_outer, shift;
+    bwd_outer(p, (blockIdx.x % per_kt) / Hkv, q_outer, kv_outer, shift);
     const int n_qt = (p.N + C::kBQ - 1) / C::kBQ;
-    const int qt_lo = p.causal ? kt : 0;  // kBQ == kBK: query steps before the diagonal see none of these keys
-    const int nq = n_qt - qt_lo;
+    // causal: query steps before the one holding the first query that reaches key kt * kBK see none
+    // of these keys
+    const int first_q = kt * C::kBK - shift;
+    const int qt_lo = (p.causal && first_q > 0) ? first_q / C::kBQ : 0;
+    const int nq = max(0, n_qt - qt_lo);
     const int n_it = p.g * nq;
 
     if (threadIdx.x == 0) {
@@ -397,8 +405,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tmem_ld32(lane_base + col_s + 32, rb);
             tmem_wait_ld();
             const int q0 = qt * C::kBQ + half * 64;  // query of column 0
-            const bool need_mask = p.causal && q0 < kt * C::kBK + C::kBK - 1;
-            const int qmin_ok = key - q0;  // columns e with q0 + e >= key are visible
+            const bool need_mask = p.causal && q0 + shift < kt * C::kBK + C::kBK - 1;
+            const int qmin_ok = key - shift - q0;  // columns e with q0 + e + shift >= key are visible
             float pf[64];
             uint32_t pk[32];
             const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
@@ -443,7 +451,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (ok) {
             // warps 0-3 write dV, warps 4-7 write dK (scale applied here)
             tc_fence_after();
-            const bool valid = key < p.N;
+            const bool valid = key < p.Nkv;
             const int64_t base = (int64_t)kv_outer * p.k_s_outer + (int64_t)hk * p.k_s_head + (int64_t)key * p.k_s_tok;
             const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
             const float mul = half == 0 ? 1.f : p.scale;
@@ -522,9 +530,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int qt = n_qt - 1 - (int)(blockIdx.x / per_qt);  // heaviest query tiles first
     const int hq = (blockIdx.x % per_qt) % p.Hq;
     const int hk = hq / p.g;
-    int q_outer, kv_outer;
-    bwd_outer(p, (blockIdx.x % per_qt) / p.Hq, q_outer, kv_outer);
-    const int kv_end = p.causal ? min(p.N, (qt + 1) * C::kBM) : p.N;
+    int q_outer, kv_outer, shift;
+    bwd_outer(p, (blockIdx.x % per_qt) / p.Hq, q_outer, kv_outer, shift);
+    // causal: keys up to the position of the tile's last query
+    const int kv_end = p.causal ? max(0, min(p.Nkv, min(p.N, (qt + 1) * C::kBM) + shift)) : p.Nkv;
     const int n_it = (kv_end + C::kBN - 1) / C::kBN;
 
     if (threadIdx.x == 0) {
@@ -640,8 +649,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc_fence_after();
             const int key0 = j * C::kBN + half * 64;  // key of this warp's column 0
             // visible columns: key0 + c <= q (causal) and key0 + c < N
-            int climit = p.N - 1 - key0;
-            if (p.causal) climit = min(climit, q - key0);
+            int climit = p.Nkv - 1 - key0;
+            if (p.causal) climit = min(climit, q + shift - key0);
             const bool need_mask = climit < 63;
             uint32_t sa[32], sb[32], da[32], db[32];
             tmem_ld32(lane_base + C::kColS + half * 64, sa);
@@ -725,6 +734,8 @@ DevBwd dev_params(const BwdParams& b) {
     p.Hq = b.q.n_head;
     p.g = b.g;
     p.N = b.q.n_tok;
+    p.Nkv = b.k.n_tok;
+    p.kv_gathered = b.kv_gathered;
     p.Npad = Npad;
     p.causal = b.causal;
     p.ring_i0 = b.ring_i0;
@@ -790,7 +801,7 @@ cudaError_t dkdv_t(const BwdParams& b, cudaStream_t stream) {
     auto kern = dkdv_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t n_kt = (b.q.n_tok + 127) / 128;
+    const int64_t n_kt = (b.k.n_tok + 127) / 128;
     const int64_t grid = n_kt * b.n_outer * (b.q.n_head / b.g);
     if (grid == 0) return cudaSuccess;
     kern<<<(unsigned)grid, kKvThreads, KvCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));

@@ -68,6 +68,7 @@ __device__ __forceinline__ uint32_t col_o(int st) { return st == 0 ? 256u : 384u
 struct DevFwd {
     int d, g, n_heads, n_outer, q_len, kv_len;
     int ring_i0, ring_t, ring_p, bsz, np;
+    int kv_gathered;
     int causal;
     float scale_log2;
     void* o_bf16;
@@ -103,9 +104,9 @@ __device__ __forceinline__ WorkItem decode_item(const DevFwd& p) {
     const int b = o % p.bsz;
     const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
     w.q_outer = i * p.bsz + b;
-    w.kv_outer = j * p.bsz + b;
+    w.kv_outer = p.kv_gathered ? b : j * p.bsz + b;
     w.q_pos0 = (long)i * p.np;
-    w.kv_pos0 = (long)j * p.np;
+    w.kv_pos0 = p.kv_gathered ? 0L : (long)j * p.np;
     w.r0 = qb * kStreams * kBM;
     w.n_max = 0;
 #pragma unroll
@@ -409,6 +410,7 @@ cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
     p.q_len = f.q_len;
     p.kv_len = f.kv_len;
     p.ring_i0 = f.ring_i0;
+    p.kv_gathered = f.kv_gathered;
     p.ring_t = f.ring_t;
     p.ring_p = f.ring_p;
     p.bsz = f.bsz;

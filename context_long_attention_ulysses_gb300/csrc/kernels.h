@@ -36,6 +36,8 @@ struct Tensor4 {
 // j = (i - ring_t) mod ring_p.  Outer index of q/o/lse: i*bsz + b; of k/v:
 // j*bsz + b.  Token positions: q i*np + token, k/v j*np + token.
 // Head-sharded layout: ring_i0 = ring_t = 0, ring_p = bsz = 1, np = 0, n_outer = 1.
+// kv_gathered = 1 (all-gather-KV): k/v hold the whole sequence per batch, outer
+// index b and token positions 0..kv_len-1, for every query rank.
 struct FwdParams {
     Tensor4 q, k, v;
     int d;
@@ -44,6 +46,7 @@ struct FwdParams {
     int n_outer;      // outer indices processed by this launch
     int q_len, kv_len;
     int ring_i0, ring_t, ring_p, bsz, np;
+    int kv_gathered;
     int causal;
     float scale;
     // epilogue: o_bf16 (bf16, strides as q) or o_f32 (float32); one is null
@@ -77,6 +80,7 @@ struct BwdParams {
     int accumulate;
     int d, g, causal;
     int ring_i0, ring_t, ring_p, bsz, n_outer;  // Ulysses: 0, 0, 1, 1, 1
+    int kv_gathered;  // all-gather-KV: k/v (and dk/dv) hold the whole sequence, outer index b
     float scale;
     int* status;
 };

@@ -210,6 +210,39 @@ usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k,
                              const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                              size_t ws_bytes, usp_stream stream);
 
+/* ---- all-gather-KV context parallelism ("Context Parallelism",
+ * ultralytics.com, "So funktioniert Kontextparallelitaet": the variant in
+ * which every rank gathers the whole K and V and attends its own query
+ * shard).  On one GPU the gather is one device copy per (rank, batch) chunk
+ * into the workspace; the attention of rank i uses global token positions
+ * (its queries are tokens i*N/P ..), so causal masking spans shards. */
+
+/* Bytes of workspace usp_allgather_attn_fwd needs: the gathered K and V
+ * (bf16, B*N*Hkv*d each) -- linear in N. */
+size_t usp_allgather_workspace_size(const usp_problem* p);
+
+/* Forward: o, lse of every rank's query shard against all keys.
+ * q, o: [P][B][N/P][Hq][d] bf16; k, v: [P][B][N/P][Hkv][d] bf16; lse: float32
+ * [P][B][N/P][Hq].  ws: at least usp_allgather_workspace_size(p) bytes,
+ * 256-byte aligned.  dtype BF16, d in {64, 128}; Hq % Hkv == 0; N % P == 0. */
+usp_status usp_allgather_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
+                                  float* lse, void* ws, size_t ws_bytes, usp_stream stream);
+
+/* Bytes of workspace usp_allgather_attn_bwd needs: the gathered K and V,
+ * 40 bytes per padded query row of every rank and head, and float32 dK, dV
+ * accumulators for the whole sequence -- linear in N. */
+size_t usp_allgather_bwd_workspace_size(const usp_problem* p);
+
+/* Backward of usp_allgather_attn_fwd: dQ_i from one pass of rank i over the
+ * gathered keys; dK and dV as the sum over ranks of each rank's partial over
+ * all keys (float32, summed in rank order: the reduce of a reduce-scatter),
+ * after which rank j keeps its shard's rows, rounded to bf16 (the scatter).
+ * Layouts as in the forward; dout, dq like q; dk, dv like k.  ws: at least
+ * usp_allgather_bwd_workspace_size(p) bytes, 256-byte aligned. */
+usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                                  size_t ws_bytes, usp_stream stream);
+
 /* Exact merge of two partial attentions over disjoint key sets, float32
  * (the merge step of ring attention):
  *   lse = ln(exp(lse_a) + exp(lse_b))

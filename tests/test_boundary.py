@@ -135,6 +135,8 @@ def test_empty_problems_enqueue_nothing(lib):
         usp.usp_attn_bwd(p, *([0] * 9), 0, 0)
         usp.usp_ring_attn_fwd(p, 0, 0, 0, 0, 0, 0, 0)
         usp.usp_ring_attn_bwd(p, *([0] * 9), 0, 0)
+        usp.usp_allgather_attn_fwd(p, 0, 0, 0, 0, 0, 0, 0)
+        usp.usp_allgather_attn_bwd(p, *([0] * 9), 0, 0)
     usp.usp_ring_merge(0, 64, 0, 0, 0, 0, 0, 0)
 
 
@@ -161,3 +163,26 @@ def test_trace_report_without_launches(lib):
     assert usp.usp_trace_report() == {}
     usp.usp_trace_enable(False)
     usp.usp_trace_reset()
+
+
+def test_allgather_argument_errors(lib):
+    p = _p()
+    ws = usp.usp_allgather_workspace_size(p)
+    bws = usp.usp_allgather_bwd_workspace_size(p)
+    assert ws == 2 * p.B * p.N * p.Hkv * p.d * 2   # gathered K and V, bf16
+    assert bws > ws
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_allgather_attn_fwd(p, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 256)
+    assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_allgather_attn_fwd(p, FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, ws)   # k not 16-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_allgather_attn_bwd(p, *([FAKE] * 9), FAKE, bws - 256)
+    assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_allgather_attn_bwd(_p(dtype="f32"), *([FAKE] * 9), FAKE, bws)
+    assert e.value.status == _lib.USP_ERR_UNSUPPORTED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_allgather_attn_fwd(_p(N=255), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws)   # N % P
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG

@@ -231,3 +231,26 @@ def test_ring_attention_backward_small(usp, orc, B, H, Hkv, N, d, P, causal):
     ref_dq, ref_dk, ref_dv, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
     _check_grads(out, ref_dq, ref_dk, ref_dv)
     _status_ok(usp)
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,P,causal", [
+    (1, 4, 4, 1024, 128, 4, True),     # four ranks of 256 tokens
+    (2, 4, 2, 1000, 64, 2, True),      # two sequences, GQA, ragged shards of 500 tokens
+    (1, 8, 2, 600, 128, 2, True),      # shards of 300 tokens: tiles straddle the rank boundary
+    (1, 4, 4, 768, 128, 3, False)])    # full attention
+def test_allgather_kv_fwd_bwd(usp, orc, B, H, Hkv, N, d, P, causal):
+    """All-gather-KV context parallelism: every rank attends its query shard against all keys."""
+    import torch
+    p = usp.Problem(B=B, Hq=H, Hkv=Hkv, N=N, d=d, P=P, causal=causal)
+    q, k, v, dO = gen((B, H, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2), gen((B, H, N, d), 3)
+    qs, ks, vs, dos = (to_dev(to_seq(x, P)) for x in (q, k, v, dO))
+    o, lse = usp.allgather_attention_fwd(p, qs, ks, vs)
+    dq, dk, dv = usp.allgather_attention_bwd(p, qs, ks, vs, o, lse, dos)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=causal)
+    lse_log = np.ascontiguousarray(to_host(lse).transpose(1, 3, 0, 2).reshape(B, H, N))
+    _check_fwd(from_seq(to_host(o)), lse_log, o_ref, lse_ref)
+    out = dict(dq=from_seq(to_host(dq)), dk=from_seq(to_host(dk)), dv=from_seq(to_host(dv)))
+    ref_dq, ref_dk, ref_dv, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
+    _check_grads(out, ref_dq, ref_dk, ref_dv)
+    _status_ok(usp)
