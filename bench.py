@@ -413,6 +413,10 @@ def run_usp(args, world, rank, local):
     if args.ring and rank == 0:
         log("ring leg")
         ring = bench_ring(usp, torch, dev, peaks)
+    allgather = None
+    if args.allgather and rank == 0:
+        log("all-gather-KV leg")
+        allgather = bench_allgather(usp, torch, dev, peaks, w)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -435,6 +439,8 @@ def run_usp(args, world, rank, local):
     }
     if ring is not None:
         line["ring"] = ring
+    if allgather is not None:
+        line["allgather_kv"] = allgather
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         log("cpu baseline (oracle)")
         line["cpu_baseline"] = cpu_baseline(w, cpu_inputs, rows_per_head=args.cpu_rows)
@@ -444,6 +450,52 @@ def run_usp(args, world, rank, local):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def bench_allgather(usp, torch, dev, peaks, w):
+    """All-gather-KV context parallelism on the step's workload: one timed forward and one timed backward."""
+    import numpy as np
+    import synth
+    p = usp.Problem(**w, causal=True)
+
+    def upload(shape, stream_id):
+        x = synth.normal(shape, seed=0, stream=stream_id, dtype="bf16")
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q = upload(p.seq_shape(w["Hq"]), synth.STREAM_Q)
+    k = upload(p.seq_shape(w["Hkv"]), synth.STREAM_K)
+    v = upload(p.seq_shape(w["Hkv"]), synth.STREAM_V)
+    dout = upload(p.seq_shape(w["Hq"]), synth.STREAM_DO)
+    o = torch.empty_like(q)
+    lse = torch.empty(p.lse_seq_shape(), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(usp.usp_allgather_workspace_size(p), usp.usp_allgather_bwd_workspace_size(p)),
+                     dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    for timed in (False, True):
+        if timed:
+            usp.usp_trace_reset()
+            usp.usp_trace_enable(True)
+        e0.record(s)
+        usp.usp_allgather_attn_fwd(p, q, k, v, o, lse, ws, None, s.cuda_stream)
+        e1.record(s)
+        usp.usp_allgather_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, None, s.cuda_stream)
+        e2.record(s)
+        torch.cuda.synchronize()
+    usp.usp_trace_enable(False)
+    trace = usp.usp_trace_report()
+    fms, bms = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    f = fwd_flops(w)
+    ok = usp.usp_device_status(s.cuda_stream) == 0
+    del q, k, v, dout, o, lse, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    return {"workload": "all-gather-KV context parallelism on the 128K-token workload, P=8 ranks",
+            "fwd_ms": fms, "fwd_TFLOPs": f / (fms * 1e-3) / 1e12, "bwd_ms": bms,
+            "bwd_TFLOPs": 2.5 * f / (bms * 1e-3) / 1e12,
+            "step_TFLOPs": 3.5 * f / ((fms + bms) * 1e-3) / 1e12,
+            "kernels_ms": {k_: v_[1] for k_, v_ in trace.items()}, "status_ok": ok,
+            "data": "seeded Philox N(0,1) bf16 (seed 0, streams Q/K/V/dO), sequence-sharded"}
 
 
 def bench_ring(usp, torch, dev, peaks):
@@ -520,6 +572,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=144, help="oracle rows per head for cpu_baseline")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="128k")
+    ap.add_argument("--no-allgather", dest="allgather", action="store_false",
+                    help="skip the all-gather-KV leg (one forward and one backward on the step's workload)")
     args = ap.parse_args()
     global WORKLOAD, WORKLOAD_NAME
     WORKLOAD, WORKLOAD_NAME = WORKLOADS[args.workload]
