@@ -31,6 +31,8 @@ __all__ = [
     "usp_ring_bwd_workspace_size", "usp_ring_attn_bwd", "ring_attention_bwd",
     "usp_allgather_workspace_size", "usp_allgather_attn_fwd", "usp_allgather_bwd_workspace_size",
     "usp_allgather_attn_bwd", "allgather_attention_fwd", "allgather_attention_bwd",
+    "usp_zigzag_shard", "usp_zigzag_unshard", "usp_zigzag_workspace_size", "usp_zigzag_bwd_workspace_size",
+    "usp_zigzag_attn_fwd", "usp_zigzag_attn_bwd", "zigzag_attention_fwd", "zigzag_attention_bwd",
 ]
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -195,6 +197,37 @@ def usp_allgather_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=No
                                                                   _ptr(ws), int(ws_bytes), _stream(stream)))
 
 
+def usp_zigzag_shard(p, hx: int, src, dst, stream=None) -> None:
+    check("usp_zigzag_shard", load().usp_zigzag_shard(_prob(p), int(hx), _ptr(src), _ptr(dst), _stream(stream)))
+
+
+def usp_zigzag_unshard(p, hx: int, src, dst, stream=None) -> None:
+    check("usp_zigzag_unshard", load().usp_zigzag_unshard(_prob(p), int(hx), _ptr(src), _ptr(dst), _stream(stream)))
+
+
+def usp_zigzag_workspace_size(p) -> int:
+    return int(load().usp_zigzag_workspace_size(_prob(p)))
+
+
+def usp_zigzag_bwd_workspace_size(p) -> int:
+    return int(load().usp_zigzag_bwd_workspace_size(_prob(p)))
+
+
+def usp_zigzag_attn_fwd(p, q, k, v, o, lse, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_zigzag_attn_fwd", load().usp_zigzag_attn_fwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                            _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def usp_zigzag_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_zigzag_attn_bwd", load().usp_zigzag_attn_bwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                            _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                                            int(ws_bytes), _stream(stream)))
+
+
 def usp_ring_merge(rows: int, d: int, o_a, lse_a, o_b, lse_b, o, lse, stream=None) -> None:
     check("usp_ring_merge", load().usp_ring_merge(int(rows), int(d), _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b),
                                                   _ptr(o), _ptr(lse), _stream(stream)))
@@ -306,6 +339,25 @@ def allgather_attention_bwd(p: Problem, q_seq, k_seq, v_seq, o_seq, lse_seq, dou
     dq, dk, dv = torch.empty_like(q_seq), torch.empty_like(k_seq), torch.empty_like(v_seq)
     ws = torch.empty(max(usp_allgather_bwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
     usp_allgather_attn_bwd(p, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq, dq, dk, dv, ws, None, stream)
+    return dq, dk, dv
+
+
+def zigzag_attention_fwd(p: Problem, q_zz, k_zz, v_zz, stream=None):
+    """Zigzag ring attention forward on zigzag-sharded buffers: returns (o_zz, lse_zz)."""
+    dev, dt = q_zz.device, p.torch_dtype
+    o = _empty(p.seq_shape(p.Hq), dt, dev)
+    lse = _empty(p.lse_seq_shape(), torch.float32, dev)
+    ws = torch.empty(max(usp_zigzag_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    usp_zigzag_attn_fwd(p, q_zz, k_zz, v_zz, o, lse, ws, None, stream)
+    return o, lse
+
+
+def zigzag_attention_bwd(p: Problem, q_zz, k_zz, v_zz, o_zz, lse_zz, dout_zz, stream=None):
+    """Zigzag ring attention backward on zigzag-sharded buffers: returns (dq, dk, dv), zigzag-sharded."""
+    dev = q_zz.device
+    dq, dk, dv = torch.empty_like(q_zz), torch.empty_like(k_zz), torch.empty_like(v_zz)
+    ws = torch.empty(max(usp_zigzag_bwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    usp_zigzag_attn_bwd(p, q_zz, k_zz, v_zz, o_zz, lse_zz, dout_zz, dq, dk, dv, ws, None, stream)
     return dq, dk, dv
 
 

@@ -30,7 +30,8 @@ SYMBOLS = (
     "usp_ring_workspace_size", "usp_ring_attn_fwd", "usp_ring_merge", "usp_device_status", "usp_status_string",
     "usp_build_info", "usp_trace_enable", "usp_trace_reset", "usp_trace_report", "usp_attn_bwd_noalloc",
     "usp_ring_bwd_workspace_size", "usp_ring_attn_bwd", "usp_allgather_workspace_size", "usp_allgather_attn_fwd",
-    "usp_allgather_bwd_workspace_size", "usp_allgather_attn_bwd",
+    "usp_allgather_bwd_workspace_size", "usp_allgather_attn_bwd", "usp_zigzag_shard", "usp_zigzag_unshard",
+    "usp_zigzag_workspace_size", "usp_zigzag_bwd_workspace_size", "usp_zigzag_attn_fwd", "usp_zigzag_attn_bwd",
 )
 
 
@@ -94,6 +95,12 @@ def load() -> ctypes.CDLL:
             "usp_allgather_attn_fwd": (ci, [P, vp, vp, vp, vp, vp, vp, sz, vp]),
             "usp_allgather_bwd_workspace_size": (sz, [P]),
             "usp_allgather_attn_bwd": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "usp_zigzag_shard": (ci, [P, ci, vp, vp, vp]),
+            "usp_zigzag_unshard": (ci, [P, ci, vp, vp, vp]),
+            "usp_zigzag_workspace_size": (sz, [P]),
+            "usp_zigzag_bwd_workspace_size": (sz, [P]),
+            "usp_zigzag_attn_fwd": (ci, [P, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "usp_zigzag_attn_bwd": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

@@ -644,6 +644,207 @@ usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const voi
     return cuda_status(e);
 }
 
+// ---- zigzag (load-balanced) ring attention
+// The sequence is cut into 2P chunks of c = N/(2P) tokens; rank r holds chunks
+// r and 2P-1-r as the two halves of its shard ([P][B][2][c][H][d]).
+static size_t zz_rows(const usp_problem* p) {
+    const size_t c = (size_t)p->N / (2 * (size_t)p->P);
+    return 2 * (size_t)p->P * p->B * p->Hq * ((c + 127) / 128 * 128);
+}
+
+static usp_status zz_check(const usp_problem* p) {
+    usp_status st = check_problem(p, false);
+    if (st != USP_OK) return st;
+    if (p->N % (2 * p->P) != 0) return USP_ERR_INVALID_ARG;
+    return USP_OK;
+}
+
+static usp_status zz_copy(const usp_problem* p, int Hx, const void* src, void* dst, bool to_zigzag,
+                          cudaStream_t s) {
+    usp_status st = zz_check(p);
+    if (st != USP_OK) return st;
+    if (Hx < 1) return USP_ERR_INVALID_ARG;
+    if (empty(p)) return USP_OK;
+    if (!src || !dst) return USP_ERR_INVALID_ARG;
+    const int P = p->P, B = p->B;
+    const size_t c = (size_t)p->N / (2 * P);
+    const size_t esz = p->dtype == USP_BF16 ? 2 : 4, chunk = c * Hx * p->d * esz;
+    const char* a = static_cast<const char*>(src);
+    char* z = static_cast<char*>(dst);
+    if (a < z + 2 * (size_t)P * B * chunk && z < a + 2 * (size_t)P * B * chunk) return USP_ERR_INVALID_ARG;
+    return cuda_status(traced("zigzag_copy", s, [&] {
+        for (int g = 0; g < 2 * P; ++g)
+            for (int b = 0; b < B; ++b) {
+                // chunk g: contiguous shard g/2, half g%2; zigzag rank (g < P ? g : 2P-1-g), half (g >= P)
+                const size_t off_c = (((size_t)(g / 2) * B + b) * 2 + g % 2) * chunk;
+                const size_t zr = g < P ? g : 2 * P - 1 - g;
+                const size_t off_z = ((zr * B + b) * 2 + (g >= P ? 1 : 0)) * chunk;
+                cudaError_t e = to_zigzag ? cudaMemcpyAsync(z + off_z, a + off_c, chunk, cudaMemcpyDeviceToDevice, s)
+                                          : cudaMemcpyAsync(z + off_c, a + off_z, chunk, cudaMemcpyDeviceToDevice, s);
+                if (e != cudaSuccess) return e;
+            }
+        return cudaSuccess;
+    }));
+}
+
+usp_status usp_zigzag_shard(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
+    return zz_copy(p, Hx, src, dst, true, static_cast<cudaStream_t>(stream));
+}
+
+usp_status usp_zigzag_unshard(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
+    return zz_copy(p, Hx, src, dst, false, static_cast<cudaStream_t>(stream));
+}
+
+size_t usp_zigzag_workspace_size(const usp_problem* p) {
+    if (zz_check(p) != USP_OK) return 0;
+    return usp_ring_workspace_size(p);
+}
+
+size_t usp_zigzag_bwd_workspace_size(const usp_problem* p) {
+    if (zz_check(p) != USP_OK) return 0;
+    const size_t q_elems = (size_t)p->B * p->N * p->Hq * p->d, k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
+    return ring_part(zz_rows(p) * 40) + ring_part(q_elems * 4) + 2 * ring_part(k_elems * 4);
+}
+
+static usp_status zz_common_checks(const usp_problem* p, std::initializer_list<const void*> ptrs, const void* ws) {
+    usp_status st = zz_check(p);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
+    if ((int64_t)p->B * p->P * 2 > 65535) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    return USP_OK;
+}
+
+usp_status usp_zigzag_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                               void* ws, size_t ws_bytes, usp_stream stream) {
+    usp_status st = zz_common_checks(p, {q, k, v, o, lse}, ws);
+    if (st != USP_OK || empty(p)) return st;
+    if (ws_bytes < usp_zigzag_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d;
+    const int c = p->N / (2 * P);
+    const size_t rows = (size_t)B * p->N * Hq;
+    float* acc_o = static_cast<float*>(ws);
+    float* part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + ring_part(rows * d * sizeof(float)));
+    float* part_l = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ring_part(rows * d * sizeof(float)));
+
+    FwdParams f{};
+    f.q = Tensor4{const_cast<void*>(q), d, (int64_t)Hq * d, (int64_t)c * Hq * d, Hq, c, 2 * P * B};
+    f.k = Tensor4{const_cast<void*>(k), d, (int64_t)Hkv * d, (int64_t)c * Hkv * d, Hkv, c, 2 * P * B};
+    f.v = Tensor4{const_cast<void*>(v), d, (int64_t)Hkv * d, (int64_t)c * Hkv * d, Hkv, c, 2 * P * B};
+    f.d = d;
+    f.g = Hq / Hkv;
+    f.n_heads = Hq;
+    f.n_outer = 2 * P * B;
+    f.q_len = c;
+    f.kv_len = c;
+    f.ring_i0 = 0;
+    f.ring_p = P;
+    f.bsz = B;
+    f.np = c;
+    f.zigzag = 1;
+    f.causal = p->causal ? 1 : 0;
+    f.scale = eff_scale(p);
+    f.o_s_head = d;
+    f.o_s_tok = (int64_t)Hq * d;
+    f.o_s_outer = (int64_t)c * Hq * d;
+    f.l_s_head = 1;
+    f.l_s_tok = Hq;
+    f.l_s_outer = (int64_t)c * Hq;
+    f.status = sp;
+    // step t, KV half kh: every rank attends both of its query chunks to chunk kh of the KV block it
+    // holds; pairs wholly in the future come out empty (LSE -inf) and merge as the identity
+    for (int t = 0; t < P; ++t)
+        for (int kh = 0; kh < 2; ++kh) {
+            const bool first = t == 0 && kh == 0;
+            f.ring_t = t;
+            f.zz_kh = kh;
+            f.o_f32 = first ? acc_o : part_o;
+            f.lse = first ? lse : part_l;
+            cudaError_t e = traced("zigzag_attn_partial", s, [&] { return launch_attn_fwd_bf16(f, s); });
+            if (e == cudaSuccess && !first)
+                e = traced("ring_merge", s, [&] {
+                    return launch_lse_merge((int64_t)rows, d, acc_o, lse, part_o, part_l, acc_o, lse, s);
+                });
+            if (e != cudaSuccess) return USP_ERR_CUDA;
+        }
+    return cuda_status(traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s); }));
+}
+
+usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                               size_t ws_bytes, usp_stream stream) {
+    usp_status st = zz_common_checks(p, {q, k, v, o, lse, dout, dq, dk, dv}, ws);
+    if (st != USP_OK || empty(p)) return st;
+    if (ws_bytes < usp_zigzag_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d;
+    const int c = p->N / (2 * P);
+    const size_t q_elems = (size_t)B * p->N * Hq * d, k_elems = (size_t)B * p->N * Hkv * d;
+    char* w = static_cast<char*>(ws);
+    float* acc_dq = reinterpret_cast<float*>(w + ring_part(zz_rows(p) * 40));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(q_elems * 4));
+    float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(k_elems * 4));
+
+    BwdParams b{};
+    const int64_t qs_tok = (int64_t)Hq * d, ks_tok = (int64_t)Hkv * d;
+    b.q = Tensor4{const_cast<void*>(q), d, qs_tok, (int64_t)c * qs_tok, Hq, c, 2 * P * B};
+    b.o = Tensor4{const_cast<void*>(o), d, qs_tok, (int64_t)c * qs_tok, Hq, c, 2 * P * B};
+    b.dout = Tensor4{const_cast<void*>(dout), d, qs_tok, (int64_t)c * qs_tok, Hq, c, 2 * P * B};
+    b.k = Tensor4{const_cast<void*>(k), d, ks_tok, (int64_t)c * ks_tok, Hkv, c, 2 * P * B};
+    b.v = Tensor4{const_cast<void*>(v), d, ks_tok, (int64_t)c * ks_tok, Hkv, c, 2 * P * B};
+    b.lse = lse;
+    b.l_s_head = 1;
+    b.l_s_tok = Hq;
+    b.l_s_outer = (int64_t)c * Hq;
+    b.ws = reinterpret_cast<float*>(w);
+    b.n_z = 2 * P * B * Hq;
+    b.dq_f32 = acc_dq;
+    b.dk_f32 = acc_dk;
+    b.dv_f32 = acc_dv;
+    b.d = d;
+    b.g = Hq / Hkv;
+    b.causal = p->causal ? 1 : 0;
+    b.ring_i0 = 0;
+    b.ring_p = P;
+    b.bsz = B;
+    b.zigzag = 1;
+    b.scale = eff_scale(p);
+    b.status = sp;
+
+    cudaError_t e = traced("zigzag_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
+    for (int t = 0; e == cudaSuccess && t < P; ++t)
+        for (int kh = 0; e == cudaSuccess && kh < 2; ++kh) {
+            b.ring_t = t;
+            b.zz_kh = kh;
+            // dK, dV of KV chunk kh, one query half at a time (each CTA owns its key rows); every KV
+            // chunk is first written at t = 0 by query half 0
+            for (int qh = 0; e == cudaSuccess && qh < 2; ++qh) {
+                b.zz_qh = qh;
+                b.n_outer = P * B;
+                b.accumulate = (t == 0 && qh == 0) ? 0 : 1;
+                e = traced("zigzag_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+            }
+            // dQ of both query halves against KV chunk kh; every query chunk is first written at t = 0, kh = 0
+            b.zz_qh = -1;
+            b.n_outer = 2 * P * B;
+            b.accumulate = (t == 0 && kh == 0) ? 0 : 1;
+            if (e == cudaSuccess) e = traced("zigzag_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
+        }
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dq, dq, (int64_t)q_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dk, dk, (int64_t)k_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dv, dv, (int64_t)k_elems, s); });
+    return cuda_status(e);
+}
+
 usp_status usp_trace_enable(int on) {
     std::lock_guard<std::mutex> lock(g_trace_mu);
     g_trace_on = on != 0;

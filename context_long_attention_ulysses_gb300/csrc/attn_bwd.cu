@@ -128,6 +128,7 @@ struct DevBwd {
     int Hq, g, N, Npad, causal;  // Hq: query heads per outer index; N: query tokens per block
     int Nkv;                     // key tokens per block
     int ring_i0, ring_t, ring_p, bsz, n_outer, kv_gathered;
+    int zigzag, zz_kh, zz_qh;  // zigzag ring: KV half of the launch, fixed query half or -1
     float scale, scale_log2;
     const float* lse2;  // [n_z][Npad], z = query outer * Hq + head
     const float* dvec;  // [n_z][Npad]
@@ -147,6 +148,25 @@ struct DevBwd {
 // the key block's (query q sees key k, both block-local, iff q + shift >= k).
 // The Ulysses path has one outer index, 0, and shift 0.
 __device__ __forceinline__ void bwd_outer(const DevBwd& p, int o, int& q_outer, int& kv_outer, int& shift) {
+    if (p.zigzag) {
+        // zigzag: rank i holds chunks i and 2P-1-i of N tokens each (outer (i*bsz + b)*2 + half)
+        int i, b, qh;
+        if (p.zz_qh >= 0) {
+            i = p.ring_i0 + o / p.bsz;
+            b = o % p.bsz;
+            qh = p.zz_qh;
+        } else {
+            i = p.ring_i0 + o / (2 * p.bsz);
+            b = (o / 2) % p.bsz;
+            qh = o & 1;
+        }
+        const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
+        q_outer = (i * p.bsz + b) * 2 + qh;
+        kv_outer = (j * p.bsz + b) * 2 + p.zz_kh;
+        const int qc = qh ? 2 * p.ring_p - 1 - i : i, kc = p.zz_kh ? 2 * p.ring_p - 1 - j : j;
+        shift = (qc - kc) * p.N;
+        return;
+    }
     const int i = p.ring_i0 + o / p.bsz, b = o % p.bsz;
     const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
     q_outer = i * p.bsz + b;
@@ -736,6 +756,9 @@ DevBwd dev_params(const BwdParams& b) {
     p.N = b.q.n_tok;
     p.Nkv = b.k.n_tok;
     p.kv_gathered = b.kv_gathered;
+    p.zigzag = b.zigzag;
+    p.zz_kh = b.zz_kh;
+    p.zz_qh = b.zz_qh;
     p.Npad = Npad;
     p.causal = b.causal;
     p.ring_i0 = b.ring_i0;

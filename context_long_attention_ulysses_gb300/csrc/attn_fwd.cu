@@ -69,6 +69,7 @@ struct DevFwd {
     int d, g, n_heads, n_outer, q_len, kv_len;
     int ring_i0, ring_t, ring_p, bsz, np;
     int kv_gathered;
+    int zigzag, zz_kh;
     int causal;
     float scale_log2;
     void* o_bf16;
@@ -100,13 +101,23 @@ __device__ __forceinline__ WorkItem decode_item(const DevFwd& p) {
     w.head = rest % p.n_heads;
     const int o = rest / p.n_heads;
     w.kv_head = w.head / p.g;
-    const int i = p.ring_i0 + o / p.bsz;
-    const int b = o % p.bsz;
-    const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
-    w.q_outer = i * p.bsz + b;
-    w.kv_outer = p.kv_gathered ? b : j * p.bsz + b;
-    w.q_pos0 = (long)i * p.np;
-    w.kv_pos0 = p.kv_gathered ? 0L : (long)j * p.np;
+    if (p.zigzag) {
+        // zigzag: rank i holds chunks i and 2P-1-i; o -> (i, b, query half)
+        const int i = p.ring_i0 + o / (2 * p.bsz), b = (o / 2) % p.bsz, qh = o & 1;
+        const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
+        w.q_outer = (i * p.bsz + b) * 2 + qh;
+        w.kv_outer = (j * p.bsz + b) * 2 + p.zz_kh;
+        w.q_pos0 = (long)(qh ? 2 * p.ring_p - 1 - i : i) * p.np;
+        w.kv_pos0 = (long)(p.zz_kh ? 2 * p.ring_p - 1 - j : j) * p.np;
+    } else {
+        const int i = p.ring_i0 + o / p.bsz;
+        const int b = o % p.bsz;
+        const int j = ((i - p.ring_t) % p.ring_p + p.ring_p) % p.ring_p;
+        w.q_outer = i * p.bsz + b;
+        w.kv_outer = p.kv_gathered ? b : j * p.bsz + b;
+        w.q_pos0 = (long)i * p.np;
+        w.kv_pos0 = p.kv_gathered ? 0L : (long)j * p.np;
+    }
     w.r0 = qb * kStreams * kBM;
     w.n_max = 0;
 #pragma unroll
@@ -411,6 +422,8 @@ cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
     p.kv_len = f.kv_len;
     p.ring_i0 = f.ring_i0;
     p.kv_gathered = f.kv_gathered;
+    p.zigzag = f.zigzag;
+    p.zz_kh = f.zz_kh;
     p.ring_t = f.ring_t;
     p.ring_p = f.ring_p;
     p.bsz = f.bsz;

@@ -38,6 +38,9 @@ struct Tensor4 {
 // Head-sharded layout: ring_i0 = ring_t = 0, ring_p = bsz = 1, np = 0, n_outer = 1.
 // kv_gathered = 1 (all-gather-KV): k/v hold the whole sequence per batch, outer
 // index b and token positions 0..kv_len-1, for every query rank.
+// zigzag = 1 (zigzag ring): every rank's shard is two chunks of np tokens, rank i
+// holding chunks i and 2P-1-i (outer index (i*bsz + b)*2 + half); o decodes to
+// (i, b, query half), the launch's KV half is zz_kh, positions are chunk * np.
 struct FwdParams {
     Tensor4 q, k, v;
     int d;
@@ -47,6 +50,7 @@ struct FwdParams {
     int q_len, kv_len;
     int ring_i0, ring_t, ring_p, bsz, np;
     int kv_gathered;
+    int zigzag, zz_kh;
     int causal;
     float scale;
     // epilogue: o_bf16 (bf16, strides as q) or o_f32 (float32); one is null
@@ -81,6 +85,9 @@ struct BwdParams {
     int d, g, causal;
     int ring_i0, ring_t, ring_p, bsz, n_outer;  // Ulysses: 0, 0, 1, 1, 1
     int kv_gathered;  // all-gather-KV: k/v (and dk/dv) hold the whole sequence, outer index b
+    // zigzag ring (as FwdParams): zz_kh is the launch's KV half; zz_qh >= 0 fixes the query half
+    // (the outer index is then (rank, batch) only), -1 takes it from the outer index
+    int zigzag, zz_kh, zz_qh;
     float scale;
     int* status;
 };

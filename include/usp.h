@@ -243,6 +243,42 @@ usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const voi
                                   const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                                   size_t ws_bytes, usp_stream stream);
 
+/* ---- zigzag (load-balanced) ring attention.  Causal ring attention over
+ * contiguous shards gives rank i i+1 of the P block pairs; the zigzag layout
+ * cuts the sequence into 2P chunks of c = N/(2P) tokens and gives rank r
+ * chunks r and 2P-1-r, so that every rank does the same work at every ring
+ * step.  The pages describe the ring without a balance; this layout is the
+ * plain balanced reading of it.
+ * Zigzag-sharded buffers: [P][B][2][c][H][d] -- rank r's shard holds chunk r
+ * then chunk 2P-1-r.  Requires N % (2P) == 0 (USP_ERR_INVALID_ARG otherwise). */
+
+/* Contiguous sequence shards ([P][B][N/P][Hx][d], as usp_a2a_seq2head reads)
+ * to zigzag shards and back: a permutation of c-token chunks, one device copy
+ * each.  dtype gives the element size; src and dst must not overlap. */
+usp_status usp_zigzag_shard(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream);
+usp_status usp_zigzag_unshard(const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream);
+
+/* Workspace of usp_zigzag_attn_fwd (equal to usp_ring_workspace_size) and of
+ * usp_zigzag_attn_bwd (40 bytes per padded query row of every chunk and head,
+ * float32 dQ, dK, dV accumulators) -- linear in N; 0 for an invalid problem. */
+size_t usp_zigzag_workspace_size(const usp_problem* p);
+size_t usp_zigzag_bwd_workspace_size(const usp_problem* p);
+
+/* Zigzag ring forward: at step t = 0..P-1 rank i holds the KV chunks of rank
+ * j = (i - t) mod P and attends both of its query chunks to each of them at
+ * global positions (pairs wholly in the future are empty), merging every
+ * partial by log-sum-exp as usp_ring_attn_fwd does.  q, o, lse, k, v in the
+ * zigzag layout (lse: float32 [P][B][2][c][Hq]).  dtype BF16, d in {64, 128}. */
+usp_status usp_zigzag_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
+                               float* lse, void* ws, size_t ws_bytes, usp_stream stream);
+
+/* Zigzag ring backward: usp_ring_attn_bwd's accumulation over the same chunk
+ * pairs (dK, dV travel with the KV chunks, dQ stays), float32, rounded once
+ * to bf16.  Layouts as in the forward. */
+usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                               size_t ws_bytes, usp_stream stream);
+
 /* Exact merge of two partial attentions over disjoint key sets, float32
  * (the merge step of ring attention):
  *   lse = ln(exp(lse_a) + exp(lse_b))

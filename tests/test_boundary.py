@@ -137,6 +137,9 @@ def test_empty_problems_enqueue_nothing(lib):
         usp.usp_ring_attn_bwd(p, *([0] * 9), 0, 0)
         usp.usp_allgather_attn_fwd(p, 0, 0, 0, 0, 0, 0, 0)
         usp.usp_allgather_attn_bwd(p, *([0] * 9), 0, 0)
+        usp.usp_zigzag_attn_fwd(p, 0, 0, 0, 0, 0, 0, 0)
+        usp.usp_zigzag_attn_bwd(p, *([0] * 9), 0, 0)
+        usp.usp_zigzag_shard(p, 4, 0, 0)
     usp.usp_ring_merge(0, 64, 0, 0, 0, 0, 0, 0)
 
 
@@ -186,3 +189,27 @@ def test_allgather_argument_errors(lib):
     with pytest.raises(usp.UspError) as e:
         usp.usp_allgather_attn_fwd(_p(N=255), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws)   # N % P
     assert e.value.status == _lib.USP_ERR_INVALID_ARG
+
+
+def test_zigzag_argument_errors(lib):
+    p = _p()
+    ws = usp.usp_zigzag_workspace_size(p)
+    bws = usp.usp_zigzag_bwd_workspace_size(p)
+    assert ws == usp.usp_ring_workspace_size(p) and bws > 0
+    odd = _p(N=p.N + p.P)                       # N % P == 0 but N % (2P) != 0
+    assert usp.usp_zigzag_workspace_size(odd) == 0
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_zigzag_attn_fwd(odd, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40)
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_zigzag_shard(odd, 4, FAKE, FAKE * 2)
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_zigzag_shard(p, 4, FAKE, FAKE + 64)   # overlapping buffers
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_zigzag_attn_fwd(p, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 256)
+    assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_zigzag_attn_bwd(p, *([FAKE] * 9), FAKE + 64, bws)   # workspace must be 256-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED

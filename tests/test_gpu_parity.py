@@ -254,3 +254,75 @@ def test_allgather_kv_fwd_bwd(usp, orc, B, H, Hkv, N, d, P, causal):
     ref_dq, ref_dk, ref_dv, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
     _check_grads(out, ref_dq, ref_dk, ref_dv)
     _status_ok(usp)
+
+
+def _zigzag_host(x_seq, P):
+    """contiguous shards [P][B][2c][H][d] -> zigzag shards (rank r: chunks r, 2P-1-r), host-side index map."""
+    Pn, B, Np, H, d = x_seq.shape
+    c = Np // 2
+    chunks = x_seq.reshape(P, B, 2, c, H, d).transpose(1, 0, 2, 3, 4, 5).reshape(B, 2 * P, c, H, d)  # [B][g]
+    out = np.empty((P, B, 2, c, H, d), dtype=x_seq.dtype)
+    for r in range(P):
+        out[r, :, 0] = chunks[:, r]
+        out[r, :, 1] = chunks[:, 2 * P - 1 - r]
+    return out.reshape(P, B, Np, H, d)
+
+
+@pytest.mark.parametrize("dtype,B,H,N,d,P", [("bf16", 1, 4, 2048, 128, 4), ("f32", 2, 3, 600, 64, 3)])
+def test_zigzag_shard_bit_exact(usp, dtype, B, H, N, d, P):
+    import torch
+    p = usp.Problem(B=B, Hq=H, Hkv=H, N=N, d=d, P=P, dtype=dtype)
+    x = gen((B, H, N, d), 5, dtype=dtype)
+    seq = to_seq(x, P)
+    src = to_dev(seq, dtype)
+    zz = torch.empty_like(src)
+    back = torch.empty_like(src)
+    usp.usp_zigzag_shard(p, H, src, zz)
+    usp.usp_zigzag_unshard(p, H, zz, back)
+    torch.cuda.synchronize()
+    assert to_host(zz).tobytes() == _zigzag_host(to_host(src), P).tobytes()
+    assert to_host(back).tobytes() == to_host(src).tobytes()
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,P,causal", [
+    (1, 4, 4, 2048, 128, 4, True),     # chunks of 256 tokens
+    (2, 4, 2, 1200, 64, 2, True),      # two sequences, GQA, chunks of 300 tokens
+    (1, 8, 2, 1536, 128, 3, True),     # three ranks, GQA group of 4
+    (1, 4, 4, 1024, 128, 2, False)])   # full attention
+def test_zigzag_ring_fwd_bwd(usp, orc, B, H, Hkv, N, d, P, causal):
+    """Zigzag ring attention (forward and backward) against the oracle, through the shard/unshard maps."""
+    import torch
+    p = usp.Problem(B=B, Hq=H, Hkv=Hkv, N=N, d=d, P=P, causal=causal)
+    q, k, v, dO = gen((B, H, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2), gen((B, H, N, d), 3)
+
+    def zz(x, h):
+        s = to_dev(to_seq(x, P))
+        out = torch.empty_like(s)
+        usp.usp_zigzag_shard(p, h, s, out)
+        return out
+
+    def unzz(x, h):
+        out = torch.empty_like(x)
+        usp.usp_zigzag_unshard(p, h, x, out)
+        return out
+
+    qz, kz, vz, doz = zz(q, H), zz(k, Hkv), zz(v, Hkv), zz(dO, H)
+    o, lse = usp.zigzag_attention_fwd(p, qz, kz, vz)
+    dq, dk, dv = usp.zigzag_attention_bwd(p, qz, kz, vz, o, lse, doz)
+    # lse through the same chunk permutation (one "head" of d = 1 is not a valid problem: permute on the host)
+    torch.cuda.synchronize()
+    o_log = from_seq(to_host(unzz(o, H)))
+    lz = to_host(lse).reshape(P, B, 2, N // (2 * P), H)
+    lse_seq = np.empty_like(lz)
+    for r in range(P):
+        for h2 in range(2):
+            g = r if h2 == 0 else 2 * P - 1 - r
+            lse_seq[g // 2, :, g % 2] = lz[r, :, h2]
+    lse_log = np.ascontiguousarray(lse_seq.reshape(P, B, N // P, H).transpose(1, 3, 0, 2).reshape(B, H, N))
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=causal)
+    _check_fwd(o_log, lse_log, o_ref, lse_ref)
+    out = dict(dq=from_seq(to_host(unzz(dq, H))), dk=from_seq(to_host(unzz(dk, Hkv))),
+               dv=from_seq(to_host(unzz(dv, Hkv))))
+    ref_dq, ref_dk, ref_dv, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
+    _check_grads(out, ref_dq, ref_dk, ref_dv)
+    _status_ok(usp)
