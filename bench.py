@@ -551,14 +551,42 @@ def bench_ring(usp, torch, dev, peaks):
     bms = e0.elapsed_time(e1)
     bf = 2.5 * f  # backward: 10*d FLOPs per visible pair against the forward's 4*d
     ok = ok and usp.usp_device_status(s.cuda_stream) == 0
-    del q, k, v, o, lse, dout, dq, dk, dv, bws
+    del bws, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+
+    # the same inputs in the zigzag layout: one timed forward and one timed backward (the kernels are warm)
+    def to_zz(x, h):
+        out = torch.empty_like(x)
+        usp.usp_zigzag_shard(p, h, x, out, s.cuda_stream)
+        return out
+    q, k, v, dout = to_zz(q, w["Hq"]), to_zz(k, w["Hkv"]), to_zz(v, w["Hkv"]), to_zz(dout, w["Hq"])
+    o = torch.empty_like(q)
+    lse = torch.empty(p.lse_seq_shape(), dtype=torch.float32, device=dev)
+    zws = torch.empty(max(usp.usp_zigzag_workspace_size(p), usp.usp_zigzag_bwd_workspace_size(p)),
+                      dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    e2 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    usp.usp_zigzag_attn_fwd(p, q, k, v, o, lse, zws, None, s.cuda_stream)
+    e1.record(s)
+    usp.usp_zigzag_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, zws, None, s.cuda_stream)
+    e2.record(s)
+    torch.cuda.synchronize()
+    zf_ms, zb_ms = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    ok = ok and usp.usp_device_status(s.cuda_stream) == 0
+    del q, k, v, o, lse, dout, dq, dk, dv, zws
     torch.cuda.empty_cache()
     return {"workload": "512K-token ring attention forward and backward, B=1, H=32, d=128, P=8 (shards of 65536)",
             "ms": ms, "TFLOPs": f / (ms * 1e-3) / 1e12, "frac_sustained": f / (ms * 1e-3) / 1e12 / peaks["bf16_sus"],
             "kernels_ms": {k_: v_[1] for k_, v_ in trace.items()},
             "bwd_ms": bms, "bwd_TFLOPs": bf / (bms * 1e-3) / 1e12,
             "bwd_frac_sustained": bf / (bms * 1e-3) / 1e12 / peaks["bf16_sus"],
-            "bwd_kernels_ms": {k_: v_[1] for k_, v_ in btrace.items()}, "status_ok": ok,
+            "bwd_kernels_ms": {k_: v_[1] for k_, v_ in btrace.items()},
+            "zigzag": {"fwd_ms": zf_ms, "fwd_TFLOPs": f / (zf_ms * 1e-3) / 1e12, "bwd_ms": zb_ms,
+                       "bwd_TFLOPs": bf / (zb_ms * 1e-3) / 1e12,
+                       "layout": "rank r holds chunks r and 2P-1-r of 2P (load-balanced causal ring)"},
+            "status_ok": ok,
             "data": "seeded Philox N(0,1) bf16 (seed 0, streams Q/K/V/dO), sequence-sharded"}
 
 

@@ -125,7 +125,7 @@ def _check_sampled_grads(q, k, v, dO, dq, dk, dv, P):
 
 
 def test_ring_512k(usp, orc):
-    """512K tokens, 32 heads, d=128, P=8 shards of 65536: ring forward and backward."""
+    """512K tokens, 32 heads, d=128, P=8 shards of 65536: ring forward and backward, zigzag forward."""
     import torch
     from oracle import rows_blas
     B, H, N, d, P = 1, 32, 524288, 128, 8
@@ -149,7 +149,20 @@ def test_ring_512k(usp, orc):
     torch.cuda.synchronize()
     assert usp.usp_device_status() == 0
     dq, dk, dv = (to_host(_logical_from_seq(x)) for x in (dq_s, dk_s, dv_s))
-    del qs, ks, vs, dos, dq_s, dk_s, dv_s
+    del dos, dq_s, dk_s, dv_s
+    # zigzag (load-balanced) ring forward on the same inputs, back to contiguous shards
+    zz = [torch.empty_like(x) for x in (qs, ks, vs)]
+    for src, dst in zip((qs, ks, vs), zz):
+        usp.usp_zigzag_shard(p, H, src, dst)
+    o_zz, _ = usp.zigzag_attention_fwd(p, *zz)
+    o_zz_seq = torch.empty_like(o_zz)
+    usp.usp_zigzag_unshard(p, H, o_zz, o_zz_seq)
+    torch.cuda.synchronize()
+    assert usp.usp_device_status() == 0
+    dz = _logical_from_seq(o_zz_seq).float() - o_full.float()
+    assert float(dz.abs().max()) < TOL_BF16_O_MAXABS
+    assert float(dz.norm() / o_full.float().norm()) < TOL_BF16_O_RELFRO
+    del qs, ks, vs, zz, o_zz, o_zz_seq, dz
     o_ring_l = _logical_from_seq(o_ring)
     lse_ring_l = lse_ring.permute(1, 3, 0, 2).reshape(B, H, N)
     # ring == one pass (both bf16 outputs of float32 arithmetic)
