@@ -38,6 +38,9 @@ WORKLOADS = {
     # smaller case of the same kernels (profiling captures): 32K tokens, 8192 per shard
     "32k": (dict(B=1, Hq=32, Hkv=8, N=32768, d=128, P=4),
             "32K-token GQA step: Ulysses all-to-all + causal GQA attention fwd+bwd"),
+    # the same step at head dimension 64 (half the MMA work per exponential)
+    "128k_d64": (dict(B=1, Hq=32, Hkv=8, N=131072, d=64, P=8),
+                 "128K-token training step at d=64: Ulysses all-to-all + causal GQA attention fwd+bwd"),
 }
 WORKLOAD, WORKLOAD_NAME = WORKLOADS["128k"]
 RING = dict(B=1, Hq=32, Hkv=32, N=524288, d=128, P=8)
@@ -51,15 +54,15 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
 # sources they were taken on: a changed kernel reports null until re-measured.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (40999906560 + 1285327360, "0b29a310bddc8634", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (63177362432 + 528116736, "aad40e7f33180e22", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (81208904192 + 1051179008, "aad40e7f33180e22", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (30031095040 + 1285728768, "10beae3e87ab7833", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (63174866688 + 527832576, "525b6f4fb7cfacef", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (71074834176 + 1051725056, "525b6f4fb7cfacef", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 
 def measured_traffic(name: str, w):
     import hashlib
-    if name not in MEASURED_TRAFFIC or w["N"] != 131072:
+    if name not in MEASURED_TRAFFIC or w["N"] != 131072 or w["d"] != 128:
         return None
     nbytes, digest, files = MEASURED_TRAFFIC[name]
     h = hashlib.sha256()
@@ -423,7 +426,8 @@ def run_usp(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME, **w, "causal": True, "parallelism": f"sp{w['P']} simulated on 1 GPU",
-                   "l2": "inputs larger than L2 (Q and dO 1 GiB, K and V 256 MiB each); no flush"},
+                   "l2": "inputs larger than L2 (Q and dO %d MiB, K and V %d MiB each, L2 129 MB); no flush"
+                         % (q_bytes >> 20, kv_bytes >> 20)},
         "pct_bf16_peak": {"burst": value / world / peaks["bf16"], "sustained": value / world / peaks["bf16_sus"],
                           "source": peaks["source"]},
         "tokens_per_s": world * w["B"] * w["N"] / (ms * 1e-3),
