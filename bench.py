@@ -159,6 +159,22 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The slowest rank's value (the whole job's time); x itself without a process group."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs its own copy of the workload (weak scaling), so the
+    job does world x the per-rank FLOPs in the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ CPU oracle
 def oracle_inputs(w, seed=0):
     """Logical Q, K, V (bf16 bits) of the workload, from the seeded generator."""
@@ -334,13 +350,6 @@ def run_usp(args, world, rank, local):
         if dist is not None:
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     def timed(fn, n):
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -349,7 +358,7 @@ def run_usp(args, world, rank, local):
             fn()
         e1.record(stream)
         barrier()
-        return max_over_ranks(e0.elapsed_time(e1))
+        return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
     log("inputs resident; warm-up")
     for _ in range(args.warmup):
@@ -369,7 +378,7 @@ def run_usp(args, world, rank, local):
     clocks = clk.summary()
     ms = total_ms / args.steps
     flops_step = 3.5 * fwd_flops(w)
-    value = world * flops_step / (ms * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, ms)
 
     # ---- end to end: host buffers in, host buffers out, every step
     log(f"timed region done ({ms:.1f} ms/step); end-to-end leg")
@@ -377,7 +386,7 @@ def run_usp(args, world, rank, local):
     e2e_ms = timed(e2e_step, args.steps) / args.steps
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+    e2e_value = job_tflops(world, flops_step, e2e_ms)
     if usp.usp_device_status(sh) != 0:
         raise RuntimeError("device status reports a timed-out wait")
 
