@@ -271,11 +271,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int Hkv = p.Hq / p.g;
-    const int per_kt = p.n_outer * Hkv;
-    const int kt = blockIdx.x / per_kt;  // low key tiles carry the most causal work: they go first
-    const int hk = (blockIdx.x % per_kt) % Hkv;
+    // group-major: all key tiles of one (outer index, KV head) -- low key tiles first, they carry the
+    // most causal work -- before the next, so that the CTAs in flight stream the same Q/dO tiles
+    const int n_kt = (p.Nkv + C::kBK - 1) / C::kBK;
+    const int grp = blockIdx.x / n_kt;
+    const int kt = blockIdx.x % n_kt;
+    const int hk = grp % Hkv;
     int q_outer, kv_outer, shift;
-    bwd_outer(p, (blockIdx.x % per_kt) / Hkv, q_outer, kv_outer, shift);
+    bwd_outer(p, grp / Hkv, q_outer, kv_outer, shift);
     const int n_qt = (p.N + C::kBQ - 1) / C::kBQ;
     // causal: query steps before the one holding the first query that reaches key kt * kBK see none
     // of these keys
@@ -546,12 +549,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int n_qt = (p.N + C::kBM - 1) / C::kBM;
-    const int per_qt = p.n_outer * p.Hq;
-    const int qt = n_qt - 1 - (int)(blockIdx.x / per_qt);  // heaviest query tiles first
-    const int hq = (blockIdx.x % per_qt) % p.Hq;
+    // group-major: all query tiles of one (outer index, KV head) group -- heaviest first, the group's
+    // query heads adjacent -- before the next group, so that the K/V tiles in flight stay in L2
+    const int n_kvh = p.Hq / p.g;
+    const int per_group = n_qt * p.g;
+    const int grp = (int)(blockIdx.x / per_group), within = (int)(blockIdx.x % per_group);
+    const int qt = n_qt - 1 - within / p.g;
+    const int hq = (grp % n_kvh) * p.g + within % p.g;
     const int hk = hq / p.g;
     int q_outer, kv_outer, shift;
-    bwd_outer(p, (blockIdx.x % per_qt) / p.Hq, q_outer, kv_outer, shift);
+    bwd_outer(p, grp / n_kvh, q_outer, kv_outer, shift);
     // causal: keys up to the position of the tile's last query
     const int kv_end = p.causal ? max(0, min(p.Nkv, min(p.N, (qt + 1) * C::kBM) + shift)) : p.Nkv;
     const int n_it = (kv_end + C::kBN - 1) / C::kBN;

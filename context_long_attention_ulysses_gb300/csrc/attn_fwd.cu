@@ -96,10 +96,16 @@ __device__ __forceinline__ WorkItem decode_item(const DevFwd& p) {
     const int item = blockIdx.x;
     WorkItem w;
     // heaviest (last) query blocks first: causal work grows with the position
-    const int qb = n_qb - 1 - item / per_block;
-    const int rest = item % per_block;
-    w.head = rest % p.n_heads;
-    const int o = rest / p.n_heads;
+    // group-major: all query blocks of one (outer index, KV head) group -- heaviest first, the
+    // group's query heads adjacent -- before the next group, so that the K/V tiles being read at any
+    // time belong to few KV heads and stay in L2
+    (void)per_block;
+    const int n_kvh = p.n_heads / p.g;
+    const int per_group = n_qb * p.g;
+    const int grp = item / per_group, within = item % per_group;
+    const int qb = n_qb - 1 - within / p.g;
+    w.head = (grp % n_kvh) * p.g + within % p.g;
+    const int o = grp / n_kvh;
     w.kv_head = w.head / p.g;
     if (p.zigzag) {
         // zigzag: rank i holds chunks i and 2P-1-i; o -> (i, b, query half)
