@@ -52,6 +52,8 @@ def _logical_from_seq(x_seq_dev):
 @pytest.mark.parametrize("B,Hq,Hkv,N,d,P", [
     (1, 32, 8, 32768, 128, 4),     # GQA long context, 8192 tokens per shard
     (1, 32, 8, 131072, 128, 8),    # 128K-token training step
+    (1, 16, 4, 32768, 64, 4),      # head dimension 64
+    (2, 8, 2, 16384, 128, 2),      # two sequences of 16K tokens, GQA group of 4
 ])
 def test_ulysses_long_context(usp, orc, B, Hq, Hkv, N, d, P):
     import torch
@@ -68,12 +70,15 @@ def test_ulysses_long_context(usp, orc, B, Hq, Hkv, N, d, P):
     assert to_host(saved["k"]).tobytes() == orc.seq2head(to_host(ks)).tobytes()
     if N <= 32768:
         assert to_host(saved["q"]).tobytes() == orc.seq2head(to_host(qs)).tobytes()
-    # with one sequence the head-sharded layout is the logical tensor itself
-    assert to_host(saved["q"]).tobytes() == q.tobytes()
-    assert to_host(_logical_from_seq(o_seq)).tobytes() == to_host(saved["o"]).tobytes()
+    # the head-sharded layout [P][B][Hq/P][N][d] is rank-major; with one sequence it is the logical tensor
+    def logical_from_head(x, H):
+        return np.ascontiguousarray(x.reshape(P, B, H // P, N, -1).transpose(1, 0, 2, 3, 4).reshape(B, H, N, -1))
+    assert logical_from_head(to_host(saved["q"]), Hq).tobytes() == q.tobytes()
+    o_head = logical_from_head(to_host(saved["o"]), Hq)
+    assert to_host(_logical_from_seq(o_seq)).tobytes() == o_head.tobytes()
 
-    o = to_host(saved["o"]).reshape(B, Hq, N, d)
-    lse = to_host(saved["lse"]).reshape(B, Hq, N)
+    o = o_head
+    lse = logical_from_head(to_host(saved["lse"]), Hq).reshape(B, Hq, N)
     dq = to_host(_logical_from_seq(dq_s))
     dk = to_host(_logical_from_seq(dk_s))
     dv = to_host(_logical_from_seq(dv_s))
