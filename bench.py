@@ -54,9 +54,9 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
 # sources they were taken on: a changed kernel reports null until re-measured.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (30031095040 + 1285728768, "10beae3e87ab7833", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (63174866688 + 527832576, "525b6f4fb7cfacef", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (71074834176 + 1051725056, "525b6f4fb7cfacef", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (2949723136 + 1165080064, "cbd26b7895961d48", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (9131987712 + 526389504, "0c2341223028f840", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (4567075328 + 1050547712, "0c2341223028f840", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 
