@@ -134,6 +134,7 @@ struct DevBwd {
     const float* dvec;  // [n_z][Npad]
     const uint4* xl;    // [n_z][Npad]: -lse / scale as three bf16 (a 16-byte row)
     const uint4* xd;    // [n_z][Npad]: -D as three bf16
+    const uint16_t* dout;    // upstream gradient, strided as q
     uint16_t *dq, *dk, *dv;  // bf16 results, or
     float *dq_f, *dk_f, *dv_f;  // float32 results (non-null), added to when acc != 0
     int acc;
@@ -507,6 +508,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 // Eight element-wise warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its
 // query rows) and key columns 64 (w / 4) .. + 63 of each step, so two warps
 // share each sub-partition and hide each other's latency.
+// dO, constant for the CTA, lives in TMEM as the A operand of dP = dO V^T
+// (loaded once by the element-wise warps), which leaves the shared memory it
+// would take to a fourth K stage: each K tile serves S(j) and, a step later,
+// dQ(j), so it holds its slot for nearly two steps.  dS is single-buffered;
+// the element-wise warps overwrite it only after dQ of the previous step.
 constexpr int kDqEwWarps = 8;
 constexpr int kDqProducerWarp = 8;
 constexpr int kDqMmaWarp = 9;
@@ -519,16 +525,16 @@ struct DqCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTile = kChunks * 128 * 128;
     // K is held until dQ's product, V only until dP's: separate rings, K deeper
-    static constexpr int kKStages = D == 64 ? 4 : 3;
+    static constexpr int kKStages = 4;
     static constexpr int kVStages = D == 64 ? 3 : 2;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffDO = kTile;
-    static constexpr int kOffK = 2 * kTile;
+    static constexpr int kOffK = kTile;
     static constexpr int kOffV = kOffK + kKStages * kTile;
     static constexpr int kOffBar = kOffV + kVStages * kTile;
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1;
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColDS0 = 256, kColDS1 = 320, kColDQ = 384;
+    // TMEM: S, dP (128 columns each), dS (bf16, 64), dO (bf16, D/2), dQ (D)
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDO = 320, kColDQ = 384;
 };
 
 template <int D>
@@ -545,7 +551,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     auto BAR = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
     const int kQFull = 0, kKFull = 1, kKEmpty = kKFull + C::kKStages, kVFull = kKEmpty + C::kKStages,
               kVEmpty = kVFull + C::kVStages, kSFull = kVEmpty + C::kVStages, kSFree = kSFull + 1,
-              kDsReady = kSFree + 1, kOReady = kDsReady + 2;
+              kDsReady = kSFree + 1, kDqDone = kDsReady + 1, kDoReady = kDqDone + 1, kOReady = kDoReady + 1;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int n_qt = (p.N + C::kBM - 1) / C::kBM;
@@ -577,7 +583,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mbar_init(BAR(kSFull), 1);
         mbar_init(BAR(kSFree), kDqEwWarps * 32);
         mbar_init(BAR(kDsReady), kDqEwWarps * 32);
-        mbar_init(BAR(kDsReady + 1), kDqEwWarps * 32);
+        mbar_init(BAR(kDqDone), 1);
+        mbar_init(BAR(kDoReady), kDqEwWarps * 32);
         mbar_init(BAR(kOReady), 1);
         fence_mbar_init();
     }
@@ -596,11 +603,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tma_prefetch_desc(&tm_do);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(BAR(kQFull), 2 * C::kTile);
-        for (int c = 0; c < C::kChunks; ++c) {
+        mbar_arrive_expect_tx(BAR(kQFull), C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(sbase + C::kOffQ + c * 16384, &tm_q, c * 64, hq, qt * C::kBM, q_outer, BAR(kQFull));
-            tma_load_4d(sbase + C::kOffDO + c * 16384, &tm_do, c * 64, hq, qt * C::kBM, q_outer, BAR(kQFull));
-        }
         for (int j = 0; j < n_it; ++j) {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
             if (j >= C::kKStages &&
@@ -622,7 +627,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         constexpr uint32_t kIdS = idesc_bf16(C::kBM, C::kBN, 0, 0);  // S = Q K^T, dP = dO V^T
         constexpr uint32_t kIdG = idesc_bf16(C::kBM, D, 0, 1);       // dQ += dS K, K MN-major
         // descriptors built once; each k-step adds its offset (address field, 16-byte units)
-        const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ, 16, 1024), ddo0 = sdesc_sw128(sbase + C::kOffDO, 16, 1024);
+        const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
         auto issue_s = [&](int j) -> bool {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
             if (!mbar_wait(BAR(kKFull + ks), (j / C::kKStages) & 1, abort_p, 32, p.status)) return false;
@@ -636,15 +641,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 mma_ss(tmem + C::kColS, dq0 + off, dk0 + off, kIdS, kk > 0);
             }
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T, dO from TMEM (16 values = 8 columns per step)
                 const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-                mma_ss(tmem + C::kColDP, ddo0 + off, dv0 + off, kIdS, kk > 0);
+                mma_ts(tmem + C::kColDP, tmem + C::kColDO + kk * 8, dv0 + off, kIdS, kk > 0);
             }
             mma_commit(BAR(kSFull));
             mma_commit(BAR(kVEmpty + vs));  // V_j is no longer needed once dP_j is done
             return true;
         };
         bool ok = mbar_wait(BAR(kQFull), 0, abort_p, 33, p.status);
+        ok = ok && mbar_wait(BAR(kDoReady), 0, abort_p, 30, p.status);
         ok = ok && issue_s(0);
         for (int j = 0; ok && j < n_it; ++j) {
             const int ks = j % C::kKStages;
@@ -652,14 +658,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 if (!mbar_wait(BAR(kSFree), j & 1, abort_p, 34, p.status)) break;
                 if (!issue_s(j + 1)) break;
             }
-            if (!mbar_wait(BAR(kDsReady + (j & 1)), (j >> 1) & 1, abort_p, 35, p.status)) break;
+            if (!mbar_wait(BAR(kDsReady), j & 1, abort_p, 35, p.status)) break;
             tc_fence_after();
             const uint64_t bk = sdesc_sw128(sbase + C::kOffK + ks * C::kTile, 16384, 1024);
-            const uint32_t ds = tmem + ((j & 1) ? C::kColDS1 : C::kColDS0);
+            const uint32_t ds = tmem + C::kColDS;
 #pragma unroll
             for (int kk = 0; kk < C::kBN / 16; ++kk)
                 mma_ts(tmem + C::kColDQ, ds + kk * 8, bk + (kk * 2048 >> 4), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(BAR(kKEmpty + ks));
+            mma_commit(BAR(kDqDone));  // dS may be overwritten
             if (j + 1 == n_it) mma_commit(BAR(kOReady));
         }
     } else if (warp < kDqEwWarps) {
@@ -670,6 +677,35 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int64_t vrow = ((int64_t)q_outer * p.Hq + hq) * p.Npad + q;  // q < Npad always
         const float lse2_r = p.lse2[vrow];
         const float dv_r = p.dvec[vrow];
+        if (n_it > 0) {
+            // this row's dO, values half * D/2 .. + D/2 - 1, into TMEM as packed bf16 (zeros past the last row)
+            constexpr int kW = D / 4;  // 32-bit words
+            uint32_t w[kW];
+            if (q < p.N) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.dout + (int64_t)q_outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)q * p.q_s_tok +
+                    half * (D / 2));
+#pragma unroll
+                for (int e = 0; e < kW / 4; ++e) {
+                    const uint4 v = src[e];
+                    w[4 * e] = v.x;
+                    w[4 * e + 1] = v.y;
+                    w[4 * e + 2] = v.z;
+                    w[4 * e + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < kW; ++e) w[e] = 0u;
+            }
+            if constexpr (kW == 32) {
+                tmem_st32(lane_base + C::kColDO + half * kW, w);
+            } else {
+                tmem_st16(lane_base + C::kColDO + half * kW, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(kDoReady));
+        }
         bool ok = true;
         for (int j = 0; j < n_it; ++j) {
             if (!mbar_wait(BAR(kSFull), j & 1, abort_p, 36, p.status)) { ok = false; break; }
@@ -706,11 +742,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 const float2 ds = mul2(pv, add2(dp, nd2));
                 dsp[e / 2] = pack_bf16(ds.x, ds.y);
             }
-            // dS (bf16) of keys 64 half .. + 63 into columns 32 half .. + 31 of this step's buffer
-            tmem_st32(lane_base + ((j & 1) ? C::kColDS1 : C::kColDS0) + half * 32, dsp);
+            // dS (bf16) of keys 64 half .. + 63 into columns 32 half .. + 31, once dQ of the previous
+            // step (which reads dS) has completed
+            if (j > 0) {
+                if (!mbar_wait(BAR(kDqDone), (j - 1) & 1, abort_p, 29, p.status)) { ok = false; break; }
+                tc_fence_after();
+            }
+            tmem_st32(lane_base + C::kColDS + half * 32, dsp);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(kDsReady + (j & 1)));
+            mbar_arrive(BAR(kDsReady));
         }
         if (ok && n_it > 0) ok = mbar_wait(BAR(kOReady), 0, abort_p, 37, p.status);
         if (ok) {
@@ -779,6 +820,7 @@ DevBwd dev_params(const BwdParams& b) {
     p.lse2 = b.ws + rows;
     p.xl = reinterpret_cast<const uint4*>(b.ws + 2 * rows);
     p.xd = p.xl + rows;
+    p.dout = static_cast<const uint16_t*>(b.dout.ptr);
     p.dq = static_cast<uint16_t*>(b.dq);
     p.dk = static_cast<uint16_t*>(b.dk);
     p.dv = static_cast<uint16_t*>(b.dv);
