@@ -38,6 +38,9 @@ WORKLOADS = {
     # smaller case of the same kernels (profiling captures): 32K tokens, 8192 per shard
     "32k": (dict(B=1, Hq=32, Hkv=8, N=32768, d=128, P=4),
             "32K-token GQA step: Ulysses all-to-all + causal GQA attention fwd+bwd"),
+    # the same step with one KV head per query head (the ring workload's head layout)
+    "128k_mha": (dict(B=1, Hq=32, Hkv=32, N=131072, d=128, P=8),
+                 "128K-token training step, 32 query and 32 KV heads: Ulysses all-to-all + causal attention fwd+bwd"),
     # the same step at head dimension 64 (half the MMA work per exponential)
     "128k_d64": (dict(B=1, Hq=32, Hkv=8, N=131072, d=64, P=8),
                  "128K-token training step at d=64: Ulysses all-to-all + causal GQA attention fwd+bwd"),
