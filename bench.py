@@ -57,9 +57,9 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
 # sources they were taken on: a changed kernel reports null until re-measured.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (2949723136 + 1165080064, "cbd26b7895961d48", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (9131987712 + 526389504, "0c2341223028f840", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (4567075328 + 1050547712, "0c2341223028f840", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (2942037504 + 1165606656, "cbd26b7895961d48", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (9134454528 + 526397184, "ce11a2c16989d35e", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (4521168640 + 1050162176, "ce11a2c16989d35e", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 
