@@ -22,11 +22,13 @@
 //             dV  += P^T dO, dK += dS^T Q           (A from TMEM, B MN-major)
 //           dK and dV stay in TMEM for the whole walk.
 //  3. dQ:   one CTA per (query head, 128-row tile) walking its visible key
-//           tiles: S = Q K^T, dP = dO V^T, dS on CUDA cores into TMEM,
-//           dQ += dS K.
-// No MMA ever writes TMEM columns that an earlier-issued MMA still reads
-// unless it is issued after that MMA (tcgen05.mma executes in issue order);
-// each kernel's comment gives its column plan.
+//           tiles: S = Q K^T, dP = dO V^T (dO held in TMEM), dS on CUDA
+//           cores into TMEM, dQ += dS K.
+// An MMA overwrites TMEM columns that another MMA reads only when it is issued
+// after that MMA (tcgen05.mma executes in issue order); the element-wise warps
+// overwrite TMEM only after their own loads of it have completed, or after a
+// barrier says the MMA that reads it is done.  Each kernel's comment gives its
+// column plan.
 #include <cmath>
 
 #include "kernels.h"
