@@ -57,22 +57,32 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
 # sources they were taken on: a changed kernel reports null until re-measured.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (2942037504 + 1165606656, "cbd26b7895961d48", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (9134454528 + 526397184, "ce11a2c16989d35e", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (4521168640 + 1050162176, "ce11a2c16989d35e", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (2942037504 + 1165606656, "7b645f2c664ab821", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (9134454528 + 526397184, "5fdea4487fa788e7", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (4521168640 + 1050162176, "5fdea4487fa788e7", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 
-def measured_traffic(name: str, w):
+def source_digest(files) -> str:
+    """Digest of kernel sources with comments and whitespace removed: a comment edit keeps a
+    measurement, any code change drops it."""
     import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "context_long_attention_ulysses_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(name: str, w):
     if name not in MEASURED_TRAFFIC or w["N"] != 131072 or w["d"] != 128:
         return None
     nbytes, digest, files = MEASURED_TRAFFIC[name]
-    h = hashlib.sha256()
-    for f in files:
-        with open(os.path.join(ROOT, "context_long_attention_ulysses_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return nbytes if h.hexdigest()[:16] == digest else None
+    return nbytes if source_digest(files) == digest else None
 
 
 def causal_pairs(N: int) -> int:
