@@ -541,8 +541,8 @@ struct DqCfg {
 
 template <int D>
 __global__ void __launch_bounds__(kDqThreads, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
+    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -602,7 +602,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (n_it > 0 && warp == kDqProducerWarp && lane == 0) {
         tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_do);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         mbar_arrive_expect_tx(BAR(kQFull), C::kTile);
@@ -892,7 +891,7 @@ cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
     const int64_t n_qt = (b.q.n_tok + 127) / 128;
     const int64_t grid = n_qt * b.n_outer * b.q.n_head;
     if (grid == 0) return cudaSuccess;
-    kern<<<(unsigned)grid, kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
+    kern<<<(unsigned)grid, kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.k, m.v, dev_params(b));
     return cudaGetLastError();
 }
 
