@@ -39,10 +39,16 @@ namespace {
 constexpr int kBM = 128;           // query rows per stream
 constexpr int kStreams = 2;        // query tiles per CTA
 constexpr int kBN = 128;           // keys per tile
-constexpr int kSoftmaxWarps = 8;   // 4 per stream
-constexpr int kProducerWarp = 8;
+constexpr int kSoftmaxWarps = 8;   // 4 per stream (warpgroups 0 and 1)
+constexpr int kProducerWarp = 8;   // warpgroup 2: producer, MMA issuer, two idle warps
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kThreads = 12 * 32;
+// Registers per thread after the set-up: the launch gives every warp 168 (65536 / 384, rounded down
+// to 8). Warpgroup 2 gives some back so the softmax warps can hold a whole S row in registers. Per
+// sub-partition (one warp of each warpgroup): 2 * 208 + 80 <= 3 * 168; per CTA 8 * 208 + 4 * 80 <= 12 * 168.
+constexpr int kSoftmaxRegs = 208;
+constexpr int kOtherRegs = 80;
+static_assert(2 * kSoftmaxRegs + kOtherRegs <= 3 * 168, "register split exceeds the launch allocation");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
@@ -186,7 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     volatile int* abort_p = &abort_flag;
-
+    // Each role's code sits inside the branch that set its register budget (so that the compiler
+    // gives it that budget); every warp of a warpgroup executes the same setmaxnreg.
+    if (warp >= kSoftmaxWarps) {
+        setmaxnreg_dec<kOtherRegs>();
     if (w.n_max > 0 && warp == kProducerWarp && lane == 0) {
         // ---------------------------------------------------------------- TMA producer
         tma_prefetch_desc(&tm_q);
@@ -269,7 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(BAR(kVEmpty + vs));
             if (k_waited) mma_commit(BAR(kKEmpty + ks1));
         }
-    } else if (warp < kSoftmaxWarps) {
+    }
+    } else {
+        setmaxnreg_inc<kSoftmaxRegs>();
         // ---------------------------------------------------------------- softmax warps
         const int quad = warp & 3;           // TMEM lane quadrant
         const int st = warp >> 2;            // stream
@@ -323,22 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_use = rescale ? m_new : m_run;
             const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
             const float msub = m_use == -INFINITY ? 0.f : m_use;
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            // column pairs in packed float32: x = S scale log2(e) - m, P = 2^x, two running pair sums
+            const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-msub, -msub);
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float2 x = fma2(make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]),
-                                          make_float2(p.scale_log2, p.scale_log2), make_float2(-msub, -msub));
-                    const float p0 = ex2_approx(x.x);
-                    const float p1 = ex2_approx(x.y);
-                    sum4[c & 3] += p0 + p1;
-                    pk[c] = pack_bf16(p0, p1);
+                    const float2 x = fma2(make_float2(s[h * 32 + 2 * c], s[h * 32 + 2 * c + 1]), c2, nm2);
+                    const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    sum2[c & 1] = add2(sum2[c & 1], pv);
+                    pk[c] = pack_bf16(pv.x, pv.y);
                 }
                 tmem_st16(scol + h * 16, pk);  // P over S: this row's S is already in registers
             }
-            l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
             if (__any_sync(0xffffffffu, rescale) && j > 0) {
                 // PV of tiles < j completed before S_j was signalled: scale O in place (warp-uniform
                 // branch for the collective TMEM access; rows that keep their max have alpha = 1)

@@ -226,6 +226,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register budget (all four warps of a warpgroup execute the same
+// one).  The increase waits until enough registers are free, so the caller
+// must make sure the decreases of the other warpgroups cover it.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
