@@ -62,7 +62,7 @@ extern "C" {
 typedef enum {
     USP_OK = 0,
     USP_ERR_INVALID_ARG = 1, /* null problem, bad sizes or divisibility */
-    USP_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. d not 64/128) */
+    USP_ERR_UNSUPPORTED = 2, /* valid request the library does not implement (e.g. d not 64/128) */
     USP_ERR_MISALIGNED = 3,  /* a pointer is NULL or not 16-byte aligned */
     USP_ERR_WORKSPACE = 4,   /* workspace too small */
     USP_ERR_CUDA = 5,        /* a CUDA runtime/driver call or launch failed */
