@@ -136,6 +136,7 @@ struct DevBwd {
     const float* dvec;  // [n_z][Npad]
     const uint4* xl;    // [n_z][Npad]: -lse / scale as three bf16 (a 16-byte row)
     const uint4* xd;    // [n_z][Npad]: -D as three bf16
+    const uint16_t* q;       // queries (pass 3 loads its tile into TMEM)
     const uint16_t* dout;    // upstream gradient, strided as q
     uint16_t *dq, *dk, *dv;  // bf16 results, or
     float *dq_f, *dk_f, *dv_f;  // float32 results (non-null), added to when acc != 0
@@ -507,14 +508,22 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ------------------------------------------------------------------ pass 3: dQ
+// One CTA per (query head, 128-row query tile), walking its visible key
+// tiles.  Q and dO are constant for the CTA: they live in TMEM (loaded once
+// by the element-wise warps) as the A operands of S = Q K^T and dP = dO V^T,
+// so the shared memory holds only the K and V rings.  K is the deeper ring:
+// a K tile serves S(j) and, a step later, dQ(j).
+// TMEM: S, dP (128 columns each), Q and dO (bf16, D/2 columns each), dQ (D).
+// dS (bf16) is written in place over the first half of each warp's 64-column
+// block of dP.  Per step the tensor core runs
+//     S(j+1) | dQ(j)  dP(j+1) | S(j+2) ...
+// and the element-wise warps compute P(j+1) from S(j+1) while dQ(j) and
+// dP(j+1) run, then dS(j+1) while S(j+2) runs.  dP(j+1) overwrites the
+// columns dQ(j) reads, so it is issued after dQ(j) (tcgen05.mma executes in
+// issue order).
 // Eight element-wise warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its
 // query rows) and key columns 64 (w / 4) .. + 63 of each step, so two warps
 // share each sub-partition and hide each other's latency.
-// dO, constant for the CTA, lives in TMEM as the A operand of dP = dO V^T
-// (loaded once by the element-wise warps), which leaves the shared memory it
-// would take to a fourth K stage: each K tile serves S(j) and, a step later,
-// dQ(j), so it holds its slot for nearly two steps.  dS is single-buffered;
-// the element-wise warps overwrite it only after dQ of the previous step.
 constexpr int kDqEwWarps = 8;
 constexpr int kDqProducerWarp = 8;
 constexpr int kDqMmaWarp = 9;
@@ -526,23 +535,47 @@ struct DqCfg {
     static constexpr int kBN = 128;  // keys per step
     static constexpr int kChunks = D / 64;
     static constexpr int kTile = kChunks * 128 * 128;
-    // K is held until dQ's product, V only until dP's: separate rings, K deeper
-    static constexpr int kKStages = 4;
-    static constexpr int kVStages = D == 64 ? 3 : 2;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kTile;
-    static constexpr int kOffV = kOffK + kKStages * kTile;
+    static constexpr int kKStages = D == 64 ? 8 : 5;
+    static constexpr int kVStages = D == 64 ? 4 : 2;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kKStages * kTile;
     static constexpr int kOffBar = kOffV + kVStages * kTile;
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 6;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
-    // TMEM: S, dP (128 columns each), dS (bf16, 64), dO (bf16, D/2), dQ (D)
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDO = 320, kColDQ = 384;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColQ = 256, kColDO = 256 + D / 2, kColDQ = 384;
 };
+
+// One 128-row operand (Q or dO) of this CTA into TMEM as packed bf16: thread
+// (lane quadrant, half) stores its row's values half * D/2 .. + D/2 - 1, zeros
+// past the last row.
+template <int D>
+__device__ __forceinline__ void rows_to_tmem(const uint16_t* base, bool valid, uint32_t taddr) {
+    constexpr int kW = D / 4;  // 32-bit words
+    uint32_t w[kW];
+    if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(base);
+#pragma unroll
+        for (int e = 0; e < kW / 4; ++e) {
+            const uint4 v = src[e];
+            w[4 * e] = v.x;
+            w[4 * e + 1] = v.y;
+            w[4 * e + 2] = v.z;
+            w[4 * e + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kW; ++e) w[e] = 0u;
+    }
+    if constexpr (kW == 32) {
+        tmem_st32(taddr, w);
+    } else {
+        tmem_st16(taddr, w);
+    }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kDqThreads, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
+    dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -551,9 +584,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     __shared__ int abort_flag;
     const uint32_t bar0 = sbase + C::kOffBar;
     auto BAR = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
-    const int kQFull = 0, kKFull = 1, kKEmpty = kKFull + C::kKStages, kVFull = kKEmpty + C::kKStages,
-              kVEmpty = kVFull + C::kVStages, kSFull = kVEmpty + C::kVStages, kSFree = kSFull + 1,
-              kDsReady = kSFree + 1, kDqDone = kDsReady + 1, kDoReady = kDqDone + 1, kOReady = kDoReady + 1;
+    const int kKFull = 0, kKEmpty = C::kKStages, kVFull = 2 * C::kKStages, kVEmpty = kVFull + C::kVStages,
+              kSFull = kVEmpty + C::kVStages, kSFree = kSFull + 1, kDPFull = kSFull + 2, kDsReady = kSFull + 3,
+              kQdoReady = kSFull + 4, kOReady = kSFull + 5;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int n_qt = (p.N + C::kBM - 1) / C::kBM;
@@ -573,7 +606,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(BAR(kQFull), 1);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(BAR(kKFull + s), 1);
             mbar_init(BAR(kKEmpty + s), 1);
@@ -584,9 +616,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         mbar_init(BAR(kSFull), 1);
         mbar_init(BAR(kSFree), kDqEwWarps * 32);
+        mbar_init(BAR(kDPFull), 1);
         mbar_init(BAR(kDsReady), kDqEwWarps * 32);
-        mbar_init(BAR(kDqDone), 1);
-        mbar_init(BAR(kDoReady), kDqEwWarps * 32);
+        mbar_init(BAR(kQdoReady), kDqEwWarps * 32);
         mbar_init(BAR(kOReady), 1);
         fence_mbar_init();
     }
@@ -601,12 +633,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     volatile int* abort_p = &abort_flag;
 
     if (n_it > 0 && warp == kDqProducerWarp && lane == 0) {
-        tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(BAR(kQFull), C::kTile);
-        for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sbase + C::kOffQ + c * 16384, &tm_q, c * 64, hq, qt * C::kBM, q_outer, BAR(kQFull));
         for (int j = 0; j < n_it; ++j) {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
             if (j >= C::kKStages &&
@@ -625,50 +653,63 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                             BAR(kVFull + vs));
         }
     } else if (n_it > 0 && warp == kDqMmaWarp && lane == 0) {
-        constexpr uint32_t kIdS = idesc_bf16(C::kBM, C::kBN, 0, 0);  // S = Q K^T, dP = dO V^T
+        constexpr uint32_t kIdS = idesc_bf16(C::kBM, C::kBN, 0, 0);  // S = Q K^T, dP = dO V^T (B K-major)
         constexpr uint32_t kIdG = idesc_bf16(C::kBM, D, 0, 1);       // dQ += dS K, K MN-major
-        // descriptors built once; each k-step adds its offset (address field, 16-byte units)
-        const uint64_t dq0 = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
+        // S(j) = Q K_j^T: A = Q from TMEM (16 values = 8 columns per k-step), B = K_j
         auto issue_s = [&](int j) -> bool {
-            const int ks = j % C::kKStages, vs = j % C::kVStages;
+            const int ks = j % C::kKStages;
             if (!mbar_wait(BAR(kKFull + ks), (j / C::kKStages) & 1, abort_p, 32, p.status)) return false;
-            if (!mbar_wait(BAR(kVFull + vs), (j / C::kVStages) & 1, abort_p, 39, p.status)) return false;
             tc_fence_after();
             const uint64_t dk0 = sdesc_sw128(sbase + C::kOffK + ks * C::kTile, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                mma_ts(tmem + C::kColS, tmem + C::kColQ + kk * 8, dk0 + off, kIdS, kk > 0);
+            }
+            mma_commit(BAR(kSFull));
+            return true;
+        };
+        // dP(j) = dO V_j^T: A = dO from TMEM, B = V_j
+        auto issue_dp = [&](int j) -> bool {
+            const int vs = j % C::kVStages;
+            if (!mbar_wait(BAR(kVFull + vs), (j / C::kVStages) & 1, abort_p, 39, p.status)) return false;
+            tc_fence_after();
             const uint64_t dv0 = sdesc_sw128(sbase + C::kOffV + vs * C::kTile, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-                mma_ss(tmem + C::kColS, dq0 + off, dk0 + off, kIdS, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T, dO from TMEM (16 values = 8 columns per step)
-                const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
                 mma_ts(tmem + C::kColDP, tmem + C::kColDO + kk * 8, dv0 + off, kIdS, kk > 0);
             }
-            mma_commit(BAR(kSFull));
+            mma_commit(BAR(kDPFull));
             mma_commit(BAR(kVEmpty + vs));  // V_j is no longer needed once dP_j is done
             return true;
         };
-        bool ok = mbar_wait(BAR(kQFull), 0, abort_p, 33, p.status);
-        ok = ok && mbar_wait(BAR(kDoReady), 0, abort_p, 30, p.status);
-        ok = ok && issue_s(0);
+        bool ok = mbar_wait(BAR(kQdoReady), 0, abort_p, 33, p.status);
+        if (ok) tc_fence_after();
+        ok = ok && issue_s(0) && issue_dp(0);
         for (int j = 0; ok && j < n_it; ++j) {
             const int ks = j % C::kKStages;
-            if (j + 1 < n_it) {
+            const bool more = j + 1 < n_it;
+            if (more) {
+                // S(j+1) overwrites S(j): after the element-wise warps have loaded it
                 if (!mbar_wait(BAR(kSFree), j & 1, abort_p, 34, p.status)) break;
                 if (!issue_s(j + 1)) break;
             }
             if (!mbar_wait(BAR(kDsReady), j & 1, abort_p, 35, p.status)) break;
             tc_fence_after();
             const uint64_t bk = sdesc_sw128(sbase + C::kOffK + ks * C::kTile, 16384, 1024);
-            const uint32_t ds = tmem + C::kColDS;
 #pragma unroll
-            for (int kk = 0; kk < C::kBN / 16; ++kk)
-                mma_ts(tmem + C::kColDQ, ds + kk * 8, bk + (kk * 2048 >> 4), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < C::kBN / 16; ++kk) {
+                // keys 16 kk .. + 15: the bf16 half of dP's 64-column block kk / 4
+                const uint32_t a = tmem + C::kColDP + (kk / 4) * 64 + (kk % 4) * 8;
+                mma_ts(tmem + C::kColDQ, a, bk + (kk * 2048 >> 4), kIdG, (j > 0 || kk > 0) ? 1u : 0u);
+            }
             mma_commit(BAR(kKEmpty + ks));
-            mma_commit(BAR(kDqDone));  // dS may be overwritten
-            if (j + 1 == n_it) mma_commit(BAR(kOReady));
+            if (more) {
+                if (!issue_dp(j + 1)) break;  // after dQ(j), which read dS from these columns
+            } else {
+                mma_commit(BAR(kOReady));
+            }
         }
     } else if (warp < kDqEwWarps) {
         const int quad = warp & 3, half = warp >> 2;
@@ -679,77 +720,63 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const float lse2_r = p.lse2[vrow];
         const float dv_r = p.dvec[vrow];
         if (n_it > 0) {
-            // this row's dO, values half * D/2 .. + D/2 - 1, into TMEM as packed bf16 (zeros past the last row)
-            constexpr int kW = D / 4;  // 32-bit words
-            uint32_t w[kW];
-            if (q < p.N) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    p.dout + (int64_t)q_outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)q * p.q_s_tok +
-                    half * (D / 2));
-#pragma unroll
-                for (int e = 0; e < kW / 4; ++e) {
-                    const uint4 v = src[e];
-                    w[4 * e] = v.x;
-                    w[4 * e + 1] = v.y;
-                    w[4 * e + 2] = v.z;
-                    w[4 * e + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < kW; ++e) w[e] = 0u;
-            }
-            if constexpr (kW == 32) {
-                tmem_st32(lane_base + C::kColDO + half * kW, w);
-            } else {
-                tmem_st16(lane_base + C::kColDO + half * kW, w);
-            }
+            // this row's Q and dO (values half * D/2 .. + D/2 - 1) into TMEM
+            const int64_t row = (int64_t)q_outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)q * p.q_s_tok +
+                                half * (D / 2);
+            rows_to_tmem<D>(p.q + row, q < p.N, lane_base + C::kColQ + half * (D / 4));
+            rows_to_tmem<D>(p.dout + row, q < p.N, lane_base + C::kColDO + half * (D / 4));
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(kDoReady));
+            mbar_arrive(BAR(kQdoReady));
         }
+        const uint32_t col_s = C::kColS + half * 64, col_dp = C::kColDP + half * 64;
         bool ok = true;
         for (int j = 0; j < n_it; ++j) {
+            // ---- P = exp2(S * scale * log2(e) - lse * log2(e)) on this warp's 64 key columns
             if (!mbar_wait(BAR(kSFull), j & 1, abort_p, 36, p.status)) { ok = false; break; }
             tc_fence_after();
+            uint32_t ra[32], rb[32];
+            tmem_ld32(lane_base + col_s, ra);
+            tmem_ld32(lane_base + col_s + 32, rb);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(BAR(kSFree));  // S(j) is in registers: S(j+1) may overwrite it
             const int key0 = j * C::kBN + half * 64;  // key of this warp's column 0
-            // visible columns: key0 + c <= q (causal) and key0 + c < N
+            // visible columns: key0 + c <= q (causal, block-local plus shift) and key0 + c < Nkv
             int climit = p.Nkv - 1 - key0;
             if (p.causal) climit = min(climit, q + shift - key0);
             const bool need_mask = climit < 63;
-            uint32_t sa[32], sb[32], da[32], db[32];
-            tmem_ld32(lane_base + C::kColS + half * 64, sa);
-            tmem_ld32(lane_base + C::kColS + half * 64 + 32, sb);
-            tmem_ld32(lane_base + C::kColDP + half * 64, da);
-            tmem_ld32(lane_base + C::kColDP + half * 64 + 32, db);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(BAR(kSFree));  // S and dP of step j are in registers: the next products may start
-            uint32_t dsp[32];
+            float pf[64];
             const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-            const float2 nl2 = make_float2(-lse2_r, -lse2_r), nd2 = make_float2(-dv_r, -dv_r);
+            const float2 nl2 = make_float2(-lse2_r, -lse2_r);
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
-                // column pairs in packed float32: x = S c - lse2, P = 2^x, dS = P (dP - D)
-                const float2 sv = make_float2(__uint_as_float(e < 32 ? sa[e] : sb[e - 32]),
-                                              __uint_as_float(e < 32 ? sa[e + 1] : sb[e - 31]));
-                const float2 dp = make_float2(__uint_as_float(e < 32 ? da[e] : db[e - 32]),
-                                              __uint_as_float(e < 32 ? da[e + 1] : db[e - 31]));
-                const float2 x = fma2(sv, c2, nl2);
-                float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                const float2 x = fma2(make_float2(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]),
+                                                  __uint_as_float(e < 32 ? ra[e + 1] : rb[e - 31])),
+                                      c2, nl2);
+                pf[e] = ex2_approx(x.x);
+                pf[e + 1] = ex2_approx(x.y);
                 if (need_mask) {
-                    if (e > climit) pv.x = 0.f;
-                    if (e + 1 > climit) pv.y = 0.f;
+                    if (e > climit) pf[e] = 0.f;
+                    if (e + 1 > climit) pf[e + 1] = 0.f;
                 }
-                const float2 ds = mul2(pv, add2(dp, nd2));
+            }
+            // ---- dS = P (dP - D), bf16, over the first 32 of this warp's dP columns
+            if (!mbar_wait(BAR(kDPFull), j & 1, abort_p, 28, p.status)) { ok = false; break; }
+            tc_fence_after();
+            tmem_ld32(lane_base + col_dp, ra);
+            tmem_ld32(lane_base + col_dp + 32, rb);
+            tmem_wait_ld();
+            const float2 nd2 = make_float2(-dv_r, -dv_r);
+            uint32_t dsp[32];
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+                const float2 dp = make_float2(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]),
+                                              __uint_as_float(e < 32 ? ra[e + 1] : rb[e - 31]));
+                const float2 ds = mul2(make_float2(pf[e], pf[e + 1]), add2(dp, nd2));
                 dsp[e / 2] = pack_bf16(ds.x, ds.y);
             }
-            // dS (bf16) of keys 64 half .. + 63 into columns 32 half .. + 31, once dQ of the previous
-            // step (which reads dS) has completed
-            if (j > 0) {
-                if (!mbar_wait(BAR(kDqDone), (j - 1) & 1, abort_p, 29, p.status)) { ok = false; break; }
-                tc_fence_after();
-            }
-            tmem_st32(lane_base + C::kColDS + half * 32, dsp);
+            tmem_st32(lane_base + col_dp, dsp);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(kDsReady));
@@ -821,6 +848,7 @@ DevBwd dev_params(const BwdParams& b) {
     p.lse2 = b.ws + rows;
     p.xl = reinterpret_cast<const uint4*>(b.ws + 2 * rows);
     p.xd = p.xl + rows;
+    p.q = static_cast<const uint16_t*>(b.q.ptr);
     p.dout = static_cast<const uint16_t*>(b.dout.ptr);
     p.dq = static_cast<uint16_t*>(b.dq);
     p.dk = static_cast<uint16_t*>(b.dk);
@@ -891,7 +919,7 @@ cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
     const int64_t n_qt = (b.q.n_tok + 127) / 128;
     const int64_t grid = n_qt * b.n_outer * b.q.n_head;
     if (grid == 0) return cudaSuccess;
-    kern<<<(unsigned)grid, kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.q, m.k, m.v, dev_params(b));
+    kern<<<(unsigned)grid, kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.k, m.v, dev_params(b));
     return cudaGetLastError();
 }
 
