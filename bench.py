@@ -57,9 +57,9 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
 # sources they were taken on: a changed kernel reports null until re-measured.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (2938320128 + 1165933824, "7b645f2c664ab821", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (9132020736 + 525971200, "6eccdd3cd9bd198c", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (4498027520 + 1050175488, "6eccdd3cd9bd198c", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (2932230912 + 1159816192, "644d5a0be1fde1cf", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (9136004864 + 526604800, "da0ad8f5c69e2d93", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (4428167680 + 1050199552, "da0ad8f5c69e2d93", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 
