@@ -486,6 +486,10 @@ def run_usp(args, world, rank, local):
     if args.allgather and rank == 0:
         log("all-gather-KV leg")
         allgather = bench_allgather(usp, torch, dev, peaks, w)
+    fused = None
+    if args.fused and rank == 0:
+        log("fused-remap and 2-D legs")
+        fused = bench_fused_and_hybrid(usp, torch, dev, peaks, w)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -511,6 +515,8 @@ def run_usp(args, world, rank, local):
         line["ring"] = ring
     if allgather is not None:
         line["allgather_kv"] = allgather
+    if fused is not None:
+        line["fused_remap"], line["hybrid_2d"] = fused
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         log("cpu baseline (oracle)")
         line["cpu_baseline"] = cpu_baseline(w, cpu_inputs, rows_per_head=args.cpu_rows)
@@ -566,6 +572,99 @@ def bench_allgather(usp, torch, dev, peaks, w):
             "step_TFLOPs": 3.5 * f / ((fms + bms) * 1e-3) / 1e12,
             "kernels_ms": {k_: v_[1] for k_, v_ in trace.items()}, "status_ok": ok,
             "data": "seeded Philox N(0,1) bf16 (seed 0, streams Q/K/V/dO), sequence-sharded"}
+
+
+def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
+    """Two variants of the step on its workload, one untimed and one timed pass each:
+    the all-to-all fused into the attention kernels (no remap launches), and 2-D sequence
+    parallelism (Ulysses inside groups of Pu = P/2 ranks, ring across the 2 groups)."""
+    import numpy as np
+    import synth
+    p = usp.Problem(**w, causal=True)
+    Hq, Hkv, P = w["Hq"], w["Hkv"], w["P"]
+
+    def upload(shape, stream_id):
+        x = synth.normal(shape, seed=0, stream=stream_id, dtype="bf16")
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q = upload(p.seq_shape(Hq), synth.STREAM_Q)
+    k = upload(p.seq_shape(Hkv), synth.STREAM_K)
+    v = upload(p.seq_shape(Hkv), synth.STREAM_V)
+    dout = upload(p.seq_shape(Hq), synth.STREAM_DO)
+    o, dq = torch.empty_like(q), torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    s = torch.cuda.current_stream()
+    sh = s.cuda_stream
+    f = fwd_flops(w)
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+
+    # ---- fused: sequence-sharded in, sequence-sharded out, three attention launches per pass
+    lse = torch.empty(p.lse_seq_shape(), dtype=torch.float32, device=dev)
+    ws = torch.empty(usp.usp_fused_attn_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    for timed in (False, True):
+        if timed:
+            usp.usp_trace_reset()
+            usp.usp_trace_enable(True)
+        e0.record(s)
+        usp.usp_fused_attn_fwd(p, q, k, v, o, lse, sh)
+        e1.record(s)
+        usp.usp_fused_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, None, sh)
+        e2.record(s)
+        torch.cuda.synchronize()
+    usp.usp_trace_enable(False)
+    ftrace = usp.usp_trace_report()
+    ffwd, fbwd = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    ok = usp.usp_device_status(sh) == 0
+    del lse, ws
+    torch.cuda.empty_cache()
+    fused = {"workload": f"{WORKLOAD_NAME}: Ulysses step with the all-to-all fused into the kernels "
+                         "(sequence-sharded operands read and written in place; no remap launches)",
+             "fwd_ms": ffwd, "bwd_ms": fbwd, "ms_per_step": ffwd + fbwd,
+             "step_TFLOPs": 3.5 * f / ((ffwd + fbwd) * 1e-3) / 1e12,
+             "frac_sustained": 3.5 * f / ((ffwd + fbwd) * 1e-3) / 1e12 / peaks["bf16_sus"],
+             "kernels_ms": {k_: v_[1] for k_, v_ in ftrace.items()},
+             "launches_per_step": sum(v_[0] for v_ in ftrace.values()), "status_ok": ok}
+
+    # ---- 2-D: all-to-all inside 2 groups of P/2 ranks, ring over the 2 groups, all-to-all back
+    Pu = max(1, P // 2)
+    hq = torch.empty(p.hybrid_shape(Hq, Pu), dtype=torch.bfloat16, device=dev)
+    hk = torch.empty(p.hybrid_shape(Hkv, Pu), dtype=torch.bfloat16, device=dev)
+    hv, hdk, hdv = torch.empty_like(hk), torch.empty_like(hk), torch.empty_like(hk)
+    ho, hdo, hdq = torch.empty_like(hq), torch.empty_like(hq), torch.empty_like(hq)
+    hlse = torch.empty(p.lse_hybrid_shape(Pu), dtype=torch.float32, device=dev)
+    hws = torch.empty(max(usp.usp_hybrid_workspace_size(p, Pu), usp.usp_hybrid_bwd_workspace_size(p, Pu)),
+                      dtype=torch.uint8, device=dev)
+    for timed in (False, True):
+        if timed:
+            usp.usp_trace_reset()
+            usp.usp_trace_enable(True)
+        e0.record(s)
+        usp.usp_hybrid_seq2head(p, Pu, Hq, q, hq, sh)
+        usp.usp_hybrid_seq2head(p, Pu, Hkv, k, hk, sh)
+        usp.usp_hybrid_seq2head(p, Pu, Hkv, v, hv, sh)
+        usp.usp_hybrid_attn_fwd(p, Pu, hq, hk, hv, ho, hlse, hws, None, sh)
+        usp.usp_hybrid_head2seq(p, Pu, Hq, ho, o, sh)
+        e1.record(s)
+        usp.usp_hybrid_seq2head(p, Pu, Hq, dout, hdo, sh)
+        usp.usp_hybrid_attn_bwd(p, Pu, hq, hk, hv, ho, hlse, hdo, hdq, hdk, hdv, hws, None, sh)
+        usp.usp_hybrid_head2seq(p, Pu, Hq, hdq, dq, sh)
+        usp.usp_hybrid_head2seq(p, Pu, Hkv, hdk, dk, sh)
+        usp.usp_hybrid_head2seq(p, Pu, Hkv, hdv, dv, sh)
+        e2.record(s)
+        torch.cuda.synchronize()
+    usp.usp_trace_enable(False)
+    htrace = usp.usp_trace_report()
+    hfwd, hbwd = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    ok = usp.usp_device_status(sh) == 0
+    del q, k, v, dout, o, dq, dk, dv, hq, hk, hv, hdk, hdv, ho, hdo, hdq, hlse, hws
+    torch.cuda.empty_cache()
+    hybrid = {"workload": f"{WORKLOAD_NAME}: 2-D sequence parallelism, Pu={Pu} Ulysses ranks x Pr={P // Pu} ring "
+                          "groups (all-to-all inside groups, ring across them, all-to-all back)",
+              "Pu": Pu, "Pr": P // Pu, "fwd_ms": hfwd, "bwd_ms": hbwd, "ms_per_step": hfwd + hbwd,
+              "step_TFLOPs": 3.5 * f / ((hfwd + hbwd) * 1e-3) / 1e12,
+              "kernels_ms": {k_: v_[1] for k_, v_ in htrace.items()},
+              "launches_per_step": sum(v_[0] for v_ in htrace.values()), "status_ok": ok}
+    return fused, hybrid
 
 
 def bench_ring(usp, torch, dev, peaks):
@@ -672,6 +771,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="128k")
     ap.add_argument("--no-allgather", dest="allgather", action="store_false",
                     help="skip the all-gather-KV leg (one forward and one backward on the step's workload)")
+    ap.add_argument("--no-fused", dest="fused", action="store_false",
+                    help="skip the fused-remap and 2-D (Ulysses x ring) legs on the step's workload")
     args = ap.parse_args()
     global WORKLOAD, WORKLOAD_NAME
     WORKLOAD, WORKLOAD_NAME = WORKLOADS[args.workload]

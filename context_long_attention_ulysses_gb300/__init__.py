@@ -33,6 +33,10 @@ __all__ = [
     "usp_allgather_attn_bwd", "allgather_attention_fwd", "allgather_attention_bwd",
     "usp_zigzag_shard", "usp_zigzag_unshard", "usp_zigzag_workspace_size", "usp_zigzag_bwd_workspace_size",
     "usp_zigzag_attn_fwd", "usp_zigzag_attn_bwd", "zigzag_attention_fwd", "zigzag_attention_bwd",
+    "usp_fused_attn_fwd", "usp_fused_attn_bwd_workspace_size", "usp_fused_attn_bwd", "fused_attention_fwd",
+    "fused_attention_bwd", "usp_hybrid_seq2head", "usp_hybrid_head2seq", "usp_hybrid_workspace_size",
+    "usp_hybrid_bwd_workspace_size", "usp_hybrid_attn_fwd", "usp_hybrid_attn_bwd", "hybrid_attention_fwd",
+    "hybrid_attention_bwd",
 ]
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -78,6 +82,13 @@ class Problem:
 
     def lse_seq_shape(self):
         return (self.P, self.B, self.N // self.P, self.Hq)
+
+    def hybrid_shape(self, H: int, Pu: int):
+        """2-D layout [P][B][H/Pu][N/Pr][d] (Pr = P/Pu ring groups of Pu Ulysses ranks)."""
+        return (self.P, self.B, H // Pu, self.N // (self.P // Pu), self.d)
+
+    def lse_hybrid_shape(self, Pu: int):
+        return (self.P, self.B, self.Hq // Pu, self.N // (self.P // Pu))
 
 
 def library_path() -> str:
@@ -228,6 +239,56 @@ def usp_zigzag_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None,
                                                             int(ws_bytes), _stream(stream)))
 
 
+def usp_fused_attn_fwd(p, q, k, v, o, lse, stream=None) -> None:
+    check("usp_fused_attn_fwd", load().usp_fused_attn_fwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                           _stream(stream)))
+
+
+def usp_fused_attn_bwd_workspace_size(p) -> int:
+    return int(load().usp_fused_attn_bwd_workspace_size(_prob(p)))
+
+
+def usp_fused_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_fused_attn_bwd", load().usp_fused_attn_bwd(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                           _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                                           int(ws_bytes), _stream(stream)))
+
+
+def usp_hybrid_seq2head(p, Pu: int, Hx: int, src, dst, stream=None) -> None:
+    check("usp_hybrid_seq2head", load().usp_hybrid_seq2head(_prob(p), int(Pu), int(Hx), _ptr(src), _ptr(dst),
+                                                             _stream(stream)))
+
+
+def usp_hybrid_head2seq(p, Pu: int, Hx: int, src, dst, stream=None) -> None:
+    check("usp_hybrid_head2seq", load().usp_hybrid_head2seq(_prob(p), int(Pu), int(Hx), _ptr(src), _ptr(dst),
+                                                             _stream(stream)))
+
+
+def usp_hybrid_workspace_size(p, Pu: int) -> int:
+    return int(load().usp_hybrid_workspace_size(_prob(p), int(Pu)))
+
+
+def usp_hybrid_bwd_workspace_size(p, Pu: int) -> int:
+    return int(load().usp_hybrid_bwd_workspace_size(_prob(p), int(Pu)))
+
+
+def usp_hybrid_attn_fwd(p, Pu: int, q, k, v, o, lse, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_hybrid_attn_fwd", load().usp_hybrid_attn_fwd(_prob(p), int(Pu), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                             _ptr(lse), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+def usp_hybrid_attn_bwd(p, Pu: int, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_hybrid_attn_bwd", load().usp_hybrid_attn_bwd(_prob(p), int(Pu), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                             _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                                             _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
 def usp_ring_merge(rows: int, d: int, o_a, lse_a, o_b, lse_b, o, lse, stream=None) -> None:
     check("usp_ring_merge", load().usp_ring_merge(int(rows), int(d), _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b),
                                                   _ptr(o), _ptr(lse), _stream(stream)))
@@ -367,4 +428,65 @@ def ring_attention_bwd(p: Problem, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq
     dq, dk, dv = torch.empty_like(q_seq), torch.empty_like(k_seq), torch.empty_like(v_seq)
     ws = torch.empty(max(usp_ring_bwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
     usp_ring_attn_bwd(p, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq, dq, dk, dv, ws, None, stream)
+    return dq, dk, dv
+
+
+def fused_attention_fwd(p: Problem, q_seq, k_seq, v_seq, stream=None):
+    """Ulysses attention with the all-to-all fused into the kernels: sequence-sharded Q, K, V in,
+    returns (o_seq, lse_seq) with the LSE as [P][B][N/P][Hq]."""
+    dev, dt = q_seq.device, p.torch_dtype
+    o = _empty(p.seq_shape(p.Hq), dt, dev)
+    lse = _empty(p.lse_seq_shape(), torch.float32, dev)
+    usp_fused_attn_fwd(p, q_seq, k_seq, v_seq, o, lse, stream)
+    return o, lse
+
+
+def fused_attention_bwd(p: Problem, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq, stream=None):
+    """Backward of :func:`fused_attention_fwd`: returns (dq_seq, dk_seq, dv_seq)."""
+    dev = q_seq.device
+    dq, dk, dv = torch.empty_like(q_seq), torch.empty_like(k_seq), torch.empty_like(v_seq)
+    ws = torch.empty(max(usp_fused_attn_bwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    usp_fused_attn_bwd(p, q_seq, k_seq, v_seq, o_seq, lse_seq, dout_seq, dq, dk, dv, ws, None, stream)
+    return dq, dk, dv
+
+
+def hybrid_attention_fwd(p: Problem, Pu: int, q_seq, k_seq, v_seq, stream=None):
+    """2-D sequence parallelism forward: all-to-all inside each group of Pu ranks, ring attention
+    across the P/Pu groups, all-to-all back.  Sequence-sharded in and out; returns (o_seq, saved)
+    with the hybrid-layout tensors and LSE the backward needs."""
+    dev, dt = q_seq.device, p.torch_dtype
+    qh = _empty(p.hybrid_shape(p.Hq, Pu), dt, dev)
+    kh = _empty(p.hybrid_shape(p.Hkv, Pu), dt, dev)
+    vh = _empty(p.hybrid_shape(p.Hkv, Pu), dt, dev)
+    oh = _empty(p.hybrid_shape(p.Hq, Pu), dt, dev)
+    lse = _empty(p.lse_hybrid_shape(Pu), torch.float32, dev)
+    o_seq = _empty(p.seq_shape(p.Hq), dt, dev)
+    ws = torch.empty(max(usp_hybrid_workspace_size(p, Pu), 256), dtype=torch.uint8, device=dev)
+    usp_hybrid_seq2head(p, Pu, p.Hq, q_seq, qh, stream)
+    usp_hybrid_seq2head(p, Pu, p.Hkv, k_seq, kh, stream)
+    usp_hybrid_seq2head(p, Pu, p.Hkv, v_seq, vh, stream)
+    usp_hybrid_attn_fwd(p, Pu, qh, kh, vh, oh, lse, ws, None, stream)
+    usp_hybrid_head2seq(p, Pu, p.Hq, oh, o_seq, stream)
+    return o_seq, {"q": qh, "k": kh, "v": vh, "o": oh, "lse": lse}
+
+
+def hybrid_attention_bwd(p: Problem, Pu: int, saved, do_seq, stream=None):
+    """Backward of :func:`hybrid_attention_fwd` for upstream gradient dO (sequence-sharded).
+
+    Returns (dq_seq, dk_seq, dv_seq)."""
+    dev, dt = do_seq.device, p.torch_dtype
+    doh = _empty(p.hybrid_shape(p.Hq, Pu), dt, dev)
+    dqh = _empty(p.hybrid_shape(p.Hq, Pu), dt, dev)
+    dkh = _empty(p.hybrid_shape(p.Hkv, Pu), dt, dev)
+    dvh = _empty(p.hybrid_shape(p.Hkv, Pu), dt, dev)
+    ws = torch.empty(max(usp_hybrid_bwd_workspace_size(p, Pu), 256), dtype=torch.uint8, device=dev)
+    usp_hybrid_seq2head(p, Pu, p.Hq, do_seq, doh, stream)
+    usp_hybrid_attn_bwd(p, Pu, saved["q"], saved["k"], saved["v"], saved["o"], saved["lse"], doh, dqh, dkh, dvh, ws,
+                        None, stream)
+    dq = _empty(p.seq_shape(p.Hq), dt, dev)
+    dk = _empty(p.seq_shape(p.Hkv), dt, dev)
+    dv = _empty(p.seq_shape(p.Hkv), dt, dev)
+    usp_hybrid_head2seq(p, Pu, p.Hq, dqh, dq, stream)
+    usp_hybrid_head2seq(p, Pu, p.Hkv, dkh, dk, stream)
+    usp_hybrid_head2seq(p, Pu, p.Hkv, dvh, dv, stream)
     return dq, dk, dv

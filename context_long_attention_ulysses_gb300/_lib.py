@@ -32,6 +32,9 @@ SYMBOLS = (
     "usp_ring_bwd_workspace_size", "usp_ring_attn_bwd", "usp_allgather_workspace_size", "usp_allgather_attn_fwd",
     "usp_allgather_bwd_workspace_size", "usp_allgather_attn_bwd", "usp_zigzag_shard", "usp_zigzag_unshard",
     "usp_zigzag_workspace_size", "usp_zigzag_bwd_workspace_size", "usp_zigzag_attn_fwd", "usp_zigzag_attn_bwd",
+    "usp_fused_attn_fwd", "usp_fused_attn_bwd_workspace_size", "usp_fused_attn_bwd", "usp_hybrid_seq2head",
+    "usp_hybrid_head2seq", "usp_hybrid_workspace_size", "usp_hybrid_bwd_workspace_size", "usp_hybrid_attn_fwd",
+    "usp_hybrid_attn_bwd",
 )
 
 
@@ -101,6 +104,15 @@ def load() -> ctypes.CDLL:
             "usp_zigzag_bwd_workspace_size": (sz, [P]),
             "usp_zigzag_attn_fwd": (ci, [P, vp, vp, vp, vp, vp, vp, sz, vp]),
             "usp_zigzag_attn_bwd": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "usp_fused_attn_fwd": (ci, [P, vp, vp, vp, vp, vp, vp]),
+            "usp_fused_attn_bwd_workspace_size": (sz, [P]),
+            "usp_fused_attn_bwd": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "usp_hybrid_seq2head": (ci, [P, ci, ci, vp, vp, vp]),
+            "usp_hybrid_head2seq": (ci, [P, ci, ci, vp, vp, vp]),
+            "usp_hybrid_workspace_size": (sz, [P, ci]),
+            "usp_hybrid_bwd_workspace_size": (sz, [P, ci]),
+            "usp_hybrid_attn_fwd": (ci, [P, ci, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "usp_hybrid_attn_bwd": (ci, [P, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

@@ -845,6 +845,316 @@ usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* 
     return cuda_status(e);
 }
 
+// ---- Ulysses attention with the all-to-all fused into the attention kernels
+// Q, K, V, O, dO, dQ, dK, dV stay in the sequence-sharded layout [P][B][N/P][H][d]
+// and the LSE in [P][B][N/P][Hq]: the kernels read and write every rank's shard in
+// place (split_pos), so no remap runs.  Per query head the work is the head-
+// sharded path's, tile for tile: the results are the remapped path's, bit for bit.
+static usp_status fused_checks(const usp_problem* p, std::initializer_list<const void*> ptrs) {
+    usp_status st = check_problem(p);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
+    if ((p->N / p->P) % 128 != 0) return USP_ERR_UNSUPPORTED;  // shards of whole 128-row tiles
+    if ((int64_t)p->B * p->P > 65535) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    return USP_OK;
+}
+
+// sequence-sharded view of one operand family with H heads
+static Tensor4 seq_view(const void* ptr, const usp_problem* p, int H) {
+    const int64_t Np = p->N / p->P, tok = (int64_t)H * p->d;
+    return Tensor4{const_cast<void*>(ptr), p->d, tok, Np * tok, H, (int)Np, p->P * p->B};
+}
+
+usp_status usp_fused_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                              usp_stream stream) {
+    usp_status st = fused_checks(p, {q, k, v, o, lse});
+    if (st != USP_OK || empty(p)) return st;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    const int B = p->B, Hq = p->Hq, d = p->d, Np = p->N / p->P;
+    FwdParams f{};
+    f.q = seq_view(q, p, Hq);
+    f.k = seq_view(k, p, p->Hkv);
+    f.v = seq_view(v, p, p->Hkv);
+    f.d = d;
+    f.g = Hq / p->Hkv;
+    f.n_heads = Hq;
+    f.n_outer = B;  // one outer index per batch, global positions 0 .. N-1
+    f.q_len = p->N;
+    f.kv_len = p->N;
+    f.ring_p = 1;
+    f.bsz = B;
+    f.split_np = Np;
+    f.split_b = B;
+    f.causal = p->causal ? 1 : 0;
+    f.scale = eff_scale(p);
+    f.o_bf16 = o;
+    f.o_s_head = d;
+    f.o_s_tok = (int64_t)Hq * d;
+    f.o_s_outer = (int64_t)Np * Hq * d;
+    f.lse = lse;
+    f.l_s_head = 1;
+    f.l_s_tok = Hq;
+    f.l_s_outer = (int64_t)Np * Hq;
+    f.status = sp;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(traced("fused_attn_fwd", s, [&] { return launch_attn_fwd_bf16(f, s); }));
+}
+
+size_t usp_fused_attn_bwd_workspace_size(const usp_problem* p) {
+    if (check_problem(p) != USP_OK) return 0;
+    return usp_attn_bwd_workspace_size(p);  // the same rows: (batch, head, position)
+}
+
+usp_status usp_fused_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                              size_t ws_bytes, usp_stream stream) {
+    usp_status st = fused_checks(p, {q, k, v, o, lse, dout, dq, dk, dv});
+    if (st != USP_OK || empty(p)) return st;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    if (ws_bytes < usp_fused_attn_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    const int B = p->B, Hq = p->Hq, Np = p->N / p->P;
+    BwdParams b{};
+    b.q = seq_view(q, p, Hq);
+    b.o = seq_view(o, p, Hq);
+    b.dout = seq_view(dout, p, Hq);
+    b.k = seq_view(k, p, p->Hkv);
+    b.v = seq_view(v, p, p->Hkv);
+    b.lse = lse;
+    b.l_s_head = 1;
+    b.l_s_tok = Hq;
+    b.l_s_outer = (int64_t)Np * Hq;
+    b.ws = static_cast<float*>(ws);
+    b.n_z = B * Hq;
+    b.dq = dq;
+    b.dk = dk;
+    b.dv = dv;
+    b.d = p->d;
+    b.g = Hq / p->Hkv;
+    b.causal = p->causal ? 1 : 0;
+    b.ring_p = 1;
+    b.bsz = B;
+    b.n_outer = B;
+    b.split_np = Np;
+    b.split_b = B;
+    b.scale = eff_scale(p);
+    b.status = sp;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = traced("fused_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
+    if (e == cudaSuccess) e = traced("fused_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+    if (e == cudaSuccess) e = traced("fused_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
+    return cuda_status(e);
+}
+
+// ---- 2-D (hybrid) sequence parallelism: Ulysses inside groups, ring across them
+// P = Pu * Pr ranks.  Ring group g (0 .. Pr-1) is the Pu consecutive ranks g*Pu ..
+// g*Pu + Pu - 1, holding the contiguous token chunk g of Nc = N/Pr tokens.  The
+// all-to-all inside a group leaves rank g*Pu + u with heads u*H/Pu .. (u+1)*H/Pu - 1
+// of chunk g: the hybrid layout [P][B][H/Pu][Nc][d] (LSE [P][B][Hq/Pu][Nc]).  The
+// ring then runs over the Pr groups, each query head meeting its KV head's chunks.
+static usp_status hybrid_check(const usp_problem* p, int Pu) {
+    usp_status st = check_problem(p, false);
+    if (st != USP_OK) return st;
+    if (Pu < 1 || p->P % Pu != 0 || p->Hq % Pu != 0 || p->Hkv % Pu != 0) return USP_ERR_INVALID_ARG;
+    return USP_OK;
+}
+
+static usp_status hybrid_a2a(int dir, const usp_problem* p, int Pu, int Hx, const void* src, void* dst,
+                             usp_stream stream) {
+    usp_status st = hybrid_check(p, Pu);
+    if (st != USP_OK) return st;
+    if (Hx != p->Hq && Hx != p->Hkv) return USP_ERR_INVALID_ARG;
+    const int row_bytes = p->d * elem_size(p->dtype);
+    if (row_bytes != 64 && row_bytes != 128 && row_bytes != 256 && row_bytes != 512) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    if (!aligned16(src) || !aligned16(dst)) return USP_ERR_MISALIGNED;
+    const size_t bytes = (size_t)p->B * Hx * (size_t)p->N * row_bytes;
+    const char* sb = static_cast<const char*>(src);
+    char* tb = static_cast<char*>(dst);
+    if (sb < tb + bytes && tb < sb + bytes) return USP_ERR_INVALID_ARG;  // overlap
+    // each group's Pu shards are one contiguous block on both sides: a Ulysses remap of Nc tokens
+    const int Pr = p->P / Pu, Nc = p->N / Pr;
+    const size_t blk = bytes / Pr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(traced(dir == 0 ? "hybrid_seq2head" : "hybrid_head2seq", s, [&] {
+        for (int g = 0; g < Pr; ++g) {
+            cudaError_t e = launch_remap(dir, sb + g * blk, tb + g * blk, p->B, Hx, Nc, Pu, row_bytes, s);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }));
+}
+
+usp_status usp_hybrid_seq2head(const usp_problem* p, int Pu, int Hx, const void* src, void* dst, usp_stream stream) {
+    return hybrid_a2a(0, p, Pu, Hx, src, dst, stream);
+}
+
+usp_status usp_hybrid_head2seq(const usp_problem* p, int Pu, int Hx, const void* src, void* dst, usp_stream stream) {
+    return hybrid_a2a(1, p, Pu, Hx, src, dst, stream);
+}
+
+static usp_status hybrid_attn_checks(const usp_problem* p, int Pu, std::initializer_list<const void*> ptrs,
+                                     const void* ws) {
+    usp_status st = hybrid_check(p, Pu);
+    if (st != USP_OK) return st;
+    if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
+    if (p->dtype != USP_BF16) return USP_ERR_UNSUPPORTED;
+    if ((int64_t)p->B * p->P > 65535) return USP_ERR_UNSUPPORTED;
+    if (empty(p)) return USP_OK;
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    return USP_OK;
+}
+
+// hybrid-layout view of one operand family with H heads (H/Pu per rank)
+static Tensor4 hybrid_view(const void* ptr, const usp_problem* p, int Pu, int H) {
+    const int64_t Nc = p->N / (p->P / Pu), Hl = H / Pu;
+    return Tensor4{const_cast<void*>(ptr), Nc * p->d, p->d, Hl * Nc * p->d, (int)Hl, (int)Nc, p->P * p->B};
+}
+
+// Forward workspace: float32 running and partial outputs and the partial LSE,
+// one row per (rank, batch, local head, token), in the hybrid layout.
+size_t usp_hybrid_workspace_size(const usp_problem* p, int Pu) {
+    if (hybrid_check(p, Pu) != USP_OK) return 0;
+    const size_t rows = (size_t)p->B * p->N * p->Hq;
+    return 2 * ring_part(rows * p->d * sizeof(float)) + ring_part(rows * sizeof(float));
+}
+
+usp_status usp_hybrid_attn_fwd(const usp_problem* p, int Pu, const void* q, const void* k, const void* v, void* o,
+                               float* lse, void* ws, size_t ws_bytes, usp_stream stream) {
+    usp_status st = hybrid_attn_checks(p, Pu, {q, k, v, o, lse}, ws);
+    if (st != USP_OK || empty(p)) return st;
+    if (ws_bytes < usp_hybrid_workspace_size(p, Pu)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Pr = p->P / Pu, B = p->B, d = p->d, Nc = p->N / Pr, Hl = p->Hq / Pu;
+    const size_t rows = (size_t)B * p->N * p->Hq;
+    const size_t rows_per_group = (size_t)Pu * B * Hl * Nc;
+    float* acc_o = static_cast<float*>(ws);
+    float* part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + ring_part(rows * d * sizeof(float)));
+    float* part_l = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * ring_part(rows * d * sizeof(float)));
+
+    // the ring decode over groups: query group i, its rank-and-batch index u*B + b as the "batch"
+    // (bsz = Pu*B), so that outer index i*Pu*B + u*B + b is rank i*Pu + u, batch b
+    FwdParams f{};
+    f.q = hybrid_view(q, p, Pu, p->Hq);
+    f.k = hybrid_view(k, p, Pu, p->Hkv);
+    f.v = hybrid_view(v, p, Pu, p->Hkv);
+    f.d = d;
+    f.g = p->Hq / p->Hkv;
+    f.n_heads = Hl;
+    f.q_len = Nc;
+    f.kv_len = Nc;
+    f.ring_p = Pr;
+    f.bsz = Pu * B;
+    f.np = Nc;
+    f.causal = p->causal ? 1 : 0;
+    f.scale = eff_scale(p);
+    f.o_s_head = (int64_t)Nc * d;
+    f.o_s_tok = d;
+    f.o_s_outer = (int64_t)Hl * Nc * d;
+    f.l_s_head = Nc;
+    f.l_s_tok = 1;
+    f.l_s_outer = (int64_t)Hl * Nc;
+    f.status = sp;
+    for (int t = 0; t < Pr; ++t) {
+        f.ring_t = t;
+        f.ring_i0 = f.causal ? t : 0;
+        f.n_outer = (f.causal ? Pr - t : Pr) * Pu * B;
+        f.o_f32 = t == 0 ? acc_o : part_o;
+        f.lse = t == 0 ? lse : part_l;
+        cudaError_t e = traced("hybrid_attn_partial", s, [&] { return launch_attn_fwd_bf16(f, s); });
+        if (e != cudaSuccess) return USP_ERR_CUDA;
+        if (t > 0) {
+            const size_t r0 = (size_t)f.ring_i0 * rows_per_group;
+            e = traced("ring_merge", s, [&] {
+                return launch_lse_merge((int64_t)(rows - r0), d, acc_o + r0 * d, lse + r0, part_o + r0 * d,
+                                        part_l + r0, acc_o + r0 * d, lse + r0, s);
+            });
+            if (e != cudaSuccess) return USP_ERR_CUDA;
+        }
+    }
+    return cuda_status(traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s); }));
+}
+
+// Backward workspace: 40 bytes per padded query row of every (rank, batch, local head), then
+// float32 accumulators for dQ, dK and dV in the hybrid layout.
+static size_t hybrid_bwd_rows(const usp_problem* p, int Pu) {
+    const size_t nc = (size_t)p->N / (p->P / Pu), npad = (nc + 127) / 128 * 128;
+    return (size_t)p->P * p->B * (p->Hq / Pu) * npad;
+}
+
+size_t usp_hybrid_bwd_workspace_size(const usp_problem* p, int Pu) {
+    if (hybrid_check(p, Pu) != USP_OK) return 0;
+    const size_t q_elems = (size_t)p->B * p->N * p->Hq * p->d, k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
+    return ring_part(hybrid_bwd_rows(p, Pu) * 40) + ring_part(q_elems * 4) + 2 * ring_part(k_elems * 4);
+}
+
+usp_status usp_hybrid_attn_bwd(const usp_problem* p, int Pu, const void* q, const void* k, const void* v,
+                               const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* ws, size_t ws_bytes, usp_stream stream) {
+    usp_status st = hybrid_attn_checks(p, Pu, {q, k, v, o, lse, dout, dq, dk, dv}, ws);
+    if (st != USP_OK || empty(p)) return st;
+    if (ws_bytes < usp_hybrid_bwd_workspace_size(p, Pu)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Pr = p->P / Pu, B = p->B, d = p->d, Nc = p->N / Pr, Hl = p->Hq / Pu;
+    const size_t q_elems = (size_t)B * p->N * p->Hq * d, k_elems = (size_t)B * p->N * p->Hkv * d;
+    char* w = static_cast<char*>(ws);
+    float* acc_dq = reinterpret_cast<float*>(w + ring_part(hybrid_bwd_rows(p, Pu) * 40));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(q_elems * 4));
+    float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(k_elems * 4));
+
+    BwdParams b{};
+    b.q = hybrid_view(q, p, Pu, p->Hq);
+    b.o = hybrid_view(o, p, Pu, p->Hq);
+    b.dout = hybrid_view(dout, p, Pu, p->Hq);
+    b.k = hybrid_view(k, p, Pu, p->Hkv);
+    b.v = hybrid_view(v, p, Pu, p->Hkv);
+    b.lse = lse;  // [P][B][Hq/Pu][Nc], the merged LSE of usp_hybrid_attn_fwd
+    b.l_s_head = Nc;
+    b.l_s_tok = 1;
+    b.l_s_outer = (int64_t)Hl * Nc;
+    b.ws = reinterpret_cast<float*>(w);
+    b.n_z = p->P * B * Hl;
+    b.dq_f32 = acc_dq;
+    b.dk_f32 = acc_dk;
+    b.dv_f32 = acc_dv;
+    b.d = d;
+    b.g = p->Hq / p->Hkv;
+    b.ring_p = Pr;
+    b.bsz = Pu * B;
+    b.scale = eff_scale(p);
+    b.status = sp;
+
+    cudaError_t e = traced("hybrid_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
+    if (e != cudaSuccess) return USP_ERR_CUDA;
+    for (int t = 0; t < Pr; ++t) {
+        // as the ring backward, over groups: dK, dV travel with the KV chunk, dQ stays
+        b.ring_t = t;
+        b.ring_i0 = p->causal ? t : 0;
+        b.n_outer = (p->causal ? Pr - t : Pr) * Pu * B;
+        b.causal = (p->causal && t == 0) ? 1 : 0;
+        b.accumulate = t > 0 ? 1 : 0;
+        e = traced("hybrid_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+        if (e == cudaSuccess) e = traced("hybrid_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
+        if (e != cudaSuccess) return USP_ERR_CUDA;
+    }
+    e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dq, dq, (int64_t)q_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dk, dk, (int64_t)k_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dv, dv, (int64_t)k_elems, s); });
+    return cuda_status(e);
+}
+
 usp_status usp_trace_enable(int on) {
     std::lock_guard<std::mutex> lock(g_trace_mu);
     g_trace_on = on != 0;

@@ -60,6 +60,7 @@ struct PreArgs {
     int64_t s_head, s_tok, s_outer;        // o / dout strides (elements)
     int64_t l_s_head, l_s_tok, l_s_outer;  // lse strides
     int heads, N, Npad, n_z;
+    int split_np, split_b;  // in place in the sequence-sharded layout (split_pos)
     float scale;
     float *dvec, *lse2;
     uint4 *xl, *xd;
@@ -68,7 +69,7 @@ struct PreArgs {
 // One warp per padded row z * Npad + n (z = outer * heads + head): dvec = dO . O
 // (fp32), lse2 = lse * log2(e), and the split rows of lse / scale (xl) and of
 // dvec (xd).
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
         return;
     }
     constexpr int kPer = D / 32;  // elements per lane (2 or 4)
-    const int64_t base = (int64_t)outer * a.s_outer + (int64_t)head * a.s_head + (int64_t)n * a.s_tok + lane * kPer;
+    const TokOuter at = split_pos(n, outer, SPLIT ? a.split_np : 0, a.split_b);
+    const int64_t base = (int64_t)at.outer * a.s_outer + (int64_t)head * a.s_head + (int64_t)at.tok * a.s_tok + lane * kPer;
     const uint16_t* __restrict__ o = a.o;
     const uint16_t* __restrict__ dout = a.dout;
     float acc = 0.f;
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-        const float l = a.lse[(int64_t)outer * a.l_s_outer + (int64_t)head * a.l_s_head + (int64_t)n * a.l_s_tok];
+        const float l = a.lse[(int64_t)at.outer * a.l_s_outer + (int64_t)head * a.l_s_head + (int64_t)at.tok * a.l_s_tok];
         dvec[row] = acc;
         lse2[row] = l * kLog2e;
         xl[row] = neg_split3(l / a.scale);
@@ -131,6 +133,7 @@ struct DevBwd {
     int Nkv;                     // key tokens per block
     int ring_i0, ring_t, ring_p, bsz, n_outer, kv_gathered;
     int zigzag, zz_kh, zz_qh;  // zigzag ring: KV half of the launch, fixed query half or -1
+    int split_np, split_b;     // in place in the sequence-sharded layout (split_pos); N, Nkv global
     float scale, scale_log2;
     const float* lse2;  // [n_z][Npad], z = query outer * Hq + head
     const float* dvec;  // [n_z][Npad]
@@ -258,7 +261,8 @@ struct KvCfg {
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 };
 
-template <int D>
+// SPLIT (this and dq_kernel): the sequence-sharded in-place addressing, compiled out otherwise
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kKvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
@@ -327,9 +331,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         mbar_arrive_expect_tx(BAR(kKvFull), 2 * C::kTile);
+        const TokOuter kv = split_pos(kt * C::kBK, kv_outer, SPLIT ? p.split_np : 0, p.split_b);
         for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_4d(sbase + C::kOffK + c * 16384, &tm_k, c * 64, hk, kt * C::kBK, kv_outer, BAR(kKvFull));
-            tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, hk, kt * C::kBK, kv_outer, BAR(kKvFull));
+            tma_load_4d(sbase + C::kOffK + c * 16384, &tm_k, c * 64, hk, kv.tok, kv.outer, BAR(kKvFull));
+            tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, hk, kv.tok, kv.outer, BAR(kKvFull));
         }
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::kStages;
@@ -339,10 +344,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 !mbar_wait(BAR(kQEmpty + s), ((it / C::kStages) - 1) & 1, abort_p, 21, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kQFull + s), 2 * C::kTile + 2 * C::kXBytes);
+            const TokOuter qa = split_pos(qt * C::kBQ, q_outer, SPLIT ? p.split_np : 0, p.split_b);
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, hq, qt * C::kBQ, q_outer,
+                tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, hq, qa.tok, qa.outer,
                             BAR(kQFull + s));
-                tma_load_4d(sbase + C::kOffDO + s * C::kTile + c * 16384, &tm_do, c * 64, hq, qt * C::kBQ, q_outer,
+                tma_load_4d(sbase + C::kOffDO + s * C::kTile + c * 16384, &tm_do, c * 64, hq, qa.tok, qa.outer,
                             BAR(kQFull + s));
             }
             const int64_t voff = ((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ;
@@ -479,7 +485,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             // warps 0-3 write dV, warps 4-7 write dK (scale applied here)
             tc_fence_after();
             const bool valid = key < p.Nkv;
-            const int64_t base = (int64_t)kv_outer * p.k_s_outer + (int64_t)hk * p.k_s_head + (int64_t)key * p.k_s_tok;
+            const TokOuter ka = split_pos(key, kv_outer, SPLIT ? p.split_np : 0, p.split_b);
+            const int64_t base = (int64_t)ka.outer * p.k_s_outer + (int64_t)hk * p.k_s_head + (int64_t)ka.tok * p.k_s_tok;
             const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
             const float mul = half == 0 ? 1.f : p.scale;
             uint16_t* out16 = half == 0 ? p.dv : p.dk;
@@ -573,7 +580,7 @@ __device__ __forceinline__ void rows_to_tmem(const uint16_t* base, bool valid, u
     }
 }
 
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
     using C = DqCfg<D>;
@@ -640,16 +647,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             if (j >= C::kKStages &&
                 !mbar_wait(BAR(kKEmpty + ks), ((j / C::kKStages) - 1) & 1, abort_p, 31, p.status))
                 break;
+            const TokOuter kv = split_pos(j * C::kBN, kv_outer, SPLIT ? p.split_np : 0, p.split_b);
             mbar_arrive_expect_tx(BAR(kKFull + ks), C::kTile);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sbase + C::kOffK + ks * C::kTile + c * 16384, &tm_k, c * 64, hk, j * C::kBN, kv_outer,
+                tma_load_4d(sbase + C::kOffK + ks * C::kTile + c * 16384, &tm_k, c * 64, hk, kv.tok, kv.outer,
                             BAR(kKFull + ks));
             if (j >= C::kVStages &&
                 !mbar_wait(BAR(kVEmpty + vs), ((j / C::kVStages) - 1) & 1, abort_p, 38, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kVFull + vs), C::kTile);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sbase + C::kOffV + vs * C::kTile + c * 16384, &tm_v, c * 64, hk, j * C::kBN, kv_outer,
+                tma_load_4d(sbase + C::kOffV + vs * C::kTile + c * 16384, &tm_v, c * 64, hk, kv.tok, kv.outer,
                             BAR(kVFull + vs));
         }
     } else if (n_it > 0 && warp == kDqMmaWarp && lane == 0) {
@@ -717,11 +725,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int q = qt * C::kBM + r;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const int64_t vrow = ((int64_t)q_outer * p.Hq + hq) * p.Npad + q;  // q < Npad always
+        const TokOuter qa = split_pos(q, q_outer, SPLIT ? p.split_np : 0, p.split_b);
         const float lse2_r = p.lse2[vrow];
         const float dv_r = p.dvec[vrow];
         if (n_it > 0) {
             // this row's Q and dO (values half * D/2 .. + D/2 - 1) into TMEM
-            const int64_t row = (int64_t)q_outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)q * p.q_s_tok +
+            const int64_t row = (int64_t)qa.outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)qa.tok * p.q_s_tok +
                                 half * (D / 2);
             rows_to_tmem<D>(p.q + row, q < p.N, lane_base + C::kColQ + half * (D / 4));
             rows_to_tmem<D>(p.dout + row, q < p.N, lane_base + C::kColDO + half * (D / 4));
@@ -787,7 +796,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tc_fence_after();
             const bool valid = q < p.N;
             const int64_t base =
-                (int64_t)q_outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)q * p.q_s_tok + half * (D / 2);
+                (int64_t)qa.outer * p.q_s_outer + (int64_t)hq * p.q_s_head + (int64_t)qa.tok * p.q_s_tok + half * (D / 2);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t rr[32];
@@ -821,7 +830,12 @@ bool make_bwd_maps(const BwdParams& b, int q_rows, BwdMaps* m) {
            make_tmap_bf16(&m->k, b.k, D, 128) && make_tmap_bf16(&m->v, b.v, D, 128);
 }
 
-int npad_of(const BwdParams& b) { return (b.q.n_tok + 127) / 128 * 128; }
+// query and key positions per outer index: the tensors' token extents, or in the sequence-sharded
+// in-place mode the whole sequence (every shard of one batch)
+int q_len_of(const BwdParams& b) { return b.split_np ? b.q.n_tok * (b.q.n_outer / b.split_b) : b.q.n_tok; }
+int kv_len_of(const BwdParams& b) { return b.split_np ? b.k.n_tok * (b.k.n_outer / b.split_b) : b.k.n_tok; }
+
+int npad_of(const BwdParams& b) { return (q_len_of(b) + 127) / 128 * 128; }
 
 DevBwd dev_params(const BwdParams& b) {
     const int Npad = npad_of(b);
@@ -829,8 +843,10 @@ DevBwd dev_params(const BwdParams& b) {
     DevBwd p;
     p.Hq = b.q.n_head;
     p.g = b.g;
-    p.N = b.q.n_tok;
-    p.Nkv = b.k.n_tok;
+    p.N = q_len_of(b);
+    p.Nkv = kv_len_of(b);
+    p.split_np = b.split_np;
+    p.split_b = b.split_b;
     p.kv_gathered = b.kv_gathered;
     p.zigzag = b.zigzag;
     p.zz_kh = b.zz_kh;
@@ -867,7 +883,7 @@ DevBwd dev_params(const BwdParams& b) {
     return p;
 }
 
-template <int D>
+template <int D, bool SPLIT>
 cudaError_t pre_t(const BwdParams& b, cudaStream_t stream) {
     const DevBwd p = dev_params(b);
     PreArgs a;
@@ -881,7 +897,9 @@ cudaError_t pre_t(const BwdParams& b, cudaStream_t stream) {
     a.l_s_tok = b.l_s_tok;
     a.l_s_outer = b.l_s_outer;
     a.heads = b.q.n_head;
-    a.N = b.q.n_tok;
+    a.N = q_len_of(b);
+    a.split_np = b.split_np;
+    a.split_b = b.split_b;
     a.Npad = p.Npad;
     a.n_z = b.n_z;
     a.scale = b.scale;
@@ -891,48 +909,63 @@ cudaError_t pre_t(const BwdParams& b, cudaStream_t stream) {
     a.xd = const_cast<uint4*>(p.xd);
     const int64_t rows = (int64_t)b.n_z * p.Npad;
     if (rows == 0) return cudaSuccess;
-    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
+    bwd_pre_kernel<D, SPLIT><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool SPLIT>
 cudaError_t dkdv_t(const BwdParams& b, cudaStream_t stream) {
     BwdMaps m;
     if (!make_bwd_maps<D>(b, KvCfg<D>::kBQ, &m)) return cudaErrorInvalidValue;
-    auto kern = dkdv_kernel<D>;
+    auto kern = dkdv_kernel<D, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t n_kt = (b.k.n_tok + 127) / 128;
+    const int64_t n_kt = (kv_len_of(b) + 127) / 128;
     const int64_t grid = n_kt * b.n_outer * (b.q.n_head / b.g);
     if (grid == 0) return cudaSuccess;
     kern<<<(unsigned)grid, kKvThreads, KvCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool SPLIT>
 cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
     BwdMaps m;
     if (!make_bwd_maps<D>(b, DqCfg<D>::kBM, &m)) return cudaErrorInvalidValue;
-    auto kern = dq_kernel<D>;
+    auto kern = dq_kernel<D, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t n_qt = (b.q.n_tok + 127) / 128;
+    const int64_t n_qt = (q_len_of(b) + 127) / 128;
     const int64_t grid = n_qt * b.n_outer * b.q.n_head;
     if (grid == 0) return cudaSuccess;
     kern<<<(unsigned)grid, kDqThreads, DqCfg<D>::kSmemBytes, stream>>>(m.k, m.v, dev_params(b));
     return cudaGetLastError();
 }
 
+// each pass in two forms: the sequence-sharded in-place addressing (split_np > 0) or not
+template <template <int, bool> class F>
+cudaError_t dispatch(const BwdParams& b, cudaStream_t stream) {
+    const bool split = b.split_np > 0;
+    if (b.d == 64) return split ? F<64, true>::run(b, stream) : F<64, false>::run(b, stream);
+    if (b.d == 128) return split ? F<128, true>::run(b, stream) : F<128, false>::run(b, stream);
+    return cudaErrorInvalidValue;
+}
+template <int D, bool S>
+struct PreF {
+    static cudaError_t run(const BwdParams& b, cudaStream_t s) { return pre_t<D, S>(b, s); }
+};
+template <int D, bool S>
+struct DkdvF {
+    static cudaError_t run(const BwdParams& b, cudaStream_t s) { return dkdv_t<D, S>(b, s); }
+};
+template <int D, bool S>
+struct DqF {
+    static cudaError_t run(const BwdParams& b, cudaStream_t s) { return dq_t<D, S>(b, s); }
+};
+
 }  // namespace
 
-cudaError_t launch_bwd_pre(const BwdParams& b, cudaStream_t stream) {
-    return b.d == 64 ? pre_t<64>(b, stream) : (b.d == 128 ? pre_t<128>(b, stream) : cudaErrorInvalidValue);
-}
-cudaError_t launch_bwd_dkdv(const BwdParams& b, cudaStream_t stream) {
-    return b.d == 64 ? dkdv_t<64>(b, stream) : (b.d == 128 ? dkdv_t<128>(b, stream) : cudaErrorInvalidValue);
-}
-cudaError_t launch_bwd_dq(const BwdParams& b, cudaStream_t stream) {
-    return b.d == 64 ? dq_t<64>(b, stream) : (b.d == 128 ? dq_t<128>(b, stream) : cudaErrorInvalidValue);
-}
+cudaError_t launch_bwd_pre(const BwdParams& b, cudaStream_t stream) { return dispatch<PreF>(b, stream); }
+cudaError_t launch_bwd_dkdv(const BwdParams& b, cudaStream_t stream) { return dispatch<DkdvF>(b, stream); }
+cudaError_t launch_bwd_dq(const BwdParams& b, cudaStream_t stream) { return dispatch<DqF>(b, stream); }
 
 }  // namespace usp

@@ -76,6 +76,7 @@ struct DevFwd {
     int ring_i0, ring_t, ring_p, bsz, np;
     int kv_gathered;
     int zigzag, zz_kh;
+    int split_np, split_b;  // > 0: read and write in place in the sequence-sharded layout (split_pos)
     int causal;
     float scale_log2;
     void* o_bf16;
@@ -147,7 +148,8 @@ __device__ __forceinline__ WorkItem decode_item(const DevFwd& p) {
     return w;
 }
 
-template <int D, bool OUT_F32>
+// SPLIT: the sequence-sharded in-place addressing (split_pos); compiled out otherwise
+template <int D, bool OUT_F32, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const DevFwd p) {
@@ -170,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const WorkItem w = decode_item(p);
+    const int snp = SPLIT ? p.split_np : 0;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -202,24 +205,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         mbar_arrive_expect_tx(BAR(kQFull), kStreams * C::kTileBytes);
-        for (int st = 0; st < kStreams; ++st)
+        for (int st = 0; st < kStreams; ++st) {
+            const TokOuter a = split_pos(w.r0 + st * kBM, w.q_outer, snp, p.split_b);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sbase + C::kOffQ + st * C::kTileBytes + c * 16384, &tm_q, c * 64, w.head,
-                            w.r0 + st * kBM, w.q_outer, BAR(kQFull));
+                tma_load_4d(sbase + C::kOffQ + st * C::kTileBytes + c * 16384, &tm_q, c * 64, w.head, a.tok, a.outer,
+                            BAR(kQFull));
+        }
+        // coordinates of key tile j; in split mode they step through the shards (whole tiles per shard)
+        TokOuter kv = {0, w.kv_outer};
         for (int j = 0; j < w.n_max; ++j) {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
             if (j >= C::kKStages && !mbar_wait(BAR(kKEmpty + ks), ((j / C::kKStages) - 1) & 1, abort_p, 1, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kKFull + ks), C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sbase + C::kOffK + ks * C::kTileBytes + c * 16384, &tm_k, c * 64, w.kv_head, j * kBN,
-                            w.kv_outer, BAR(kKFull + ks));
+                tma_load_4d(sbase + C::kOffK + ks * C::kTileBytes + c * 16384, &tm_k, c * 64, w.kv_head, kv.tok,
+                            kv.outer, BAR(kKFull + ks));
             if (j >= C::kVStages && !mbar_wait(BAR(kVEmpty + vs), ((j / C::kVStages) - 1) & 1, abort_p, 2, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kVFull + vs), C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sbase + C::kOffV + vs * C::kTileBytes + c * 16384, &tm_v, c * 64, w.kv_head, j * kBN,
-                            w.kv_outer, BAR(kVFull + vs));
+                tma_load_4d(sbase + C::kOffV + vs * C::kTileBytes + c * 16384, &tm_v, c * 64, w.kv_head, kv.tok,
+                            kv.outer, BAR(kVFull + vs));
+            kv.tok += kBN;
+            if (SPLIT && kv.tok == p.split_np) {
+                kv.tok = 0;
+                kv.outer += p.split_b;
+            }
         }
     } else if (w.n_max > 0 && warp == kMmaWarp && lane == 0) {
         // ---------------------------------------------------------------- MMA issuer
@@ -376,9 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool has = n_tiles > 0 && l_run > 0.f;
             const float inv = has ? 1.f / l_run : 0.f;
             const float lse_v = has ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
-            const int tok = r0 + row;
-            const bool valid = tok < p.q_len;
-            const int64_t obase = (int64_t)w.head * p.o_s_head + (int64_t)tok * p.o_s_tok + (int64_t)w.q_outer * p.o_s_outer;
+            const bool valid = r0 + row < p.q_len;
+            // the stream's 128 rows lie in one shard (split mode): split its first row once
+            const TokOuter a = split_pos(r0, w.q_outer, snp, p.split_b);
+            const int64_t obase =
+                (int64_t)w.head * p.o_s_head + (int64_t)(a.tok + row) * p.o_s_tok + (int64_t)a.outer * p.o_s_outer;
+            const int64_t lbase =
+                (int64_t)w.head * p.l_s_head + (int64_t)(a.tok + row) * p.l_s_tok + (int64_t)a.outer * p.l_s_outer;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -411,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (valid)
-                p.lse[(int64_t)w.head * p.l_s_head + (int64_t)tok * p.l_s_tok + (int64_t)w.q_outer * p.l_s_outer] = lse_v;
+                p.lse[lbase] = lse_v;
         }
     }
     // ---------------------------------------------------------------- teardown
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool SPLIT>
 cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
     using C = FwdCfg<D>;
     CUtensorMap tq, tk, tv;
@@ -441,6 +457,8 @@ cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
     p.kv_gathered = f.kv_gathered;
     p.zigzag = f.zigzag;
     p.zz_kh = f.zz_kh;
+    p.split_np = f.split_np;
+    p.split_b = f.split_b;
     p.ring_t = f.ring_t;
     p.ring_p = f.ring_p;
     p.bsz = f.bsz;
@@ -457,7 +475,7 @@ cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
     p.l_s_tok = f.l_s_tok;
     p.l_s_outer = f.l_s_outer;
     p.status = f.status;
-    auto kern = attn_fwd_kernel<D, OUT_F32>;
+    auto kern = attn_fwd_kernel<D, OUT_F32, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const long n_qb = (f.q_len + kStreams * kBM - 1) / (kStreams * kBM);
@@ -471,8 +489,14 @@ cudaError_t launch_fwd_t(const FwdParams& f, cudaStream_t stream) {
 
 cudaError_t launch_attn_fwd_bf16(const FwdParams& f, cudaStream_t stream) {
     const bool f32 = f.o_f32 != nullptr;
-    if (f.d == 64) return f32 ? launch_fwd_t<64, true>(f, stream) : launch_fwd_t<64, false>(f, stream);
-    if (f.d == 128) return f32 ? launch_fwd_t<128, true>(f, stream) : launch_fwd_t<128, false>(f, stream);
+    if (f.split_np > 0) {  // in place in the sequence-sharded layout: bf16 output only
+        if (f32) return cudaErrorInvalidValue;
+        if (f.d == 64) return launch_fwd_t<64, false, true>(f, stream);
+        if (f.d == 128) return launch_fwd_t<128, false, true>(f, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (f.d == 64) return f32 ? launch_fwd_t<64, true, false>(f, stream) : launch_fwd_t<64, false, false>(f, stream);
+    if (f.d == 128) return f32 ? launch_fwd_t<128, true, false>(f, stream) : launch_fwd_t<128, false, false>(f, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -41,6 +41,13 @@ struct Tensor4 {
 // zigzag = 1 (zigzag ring): every rank's shard is two chunks of np tokens, rank i
 // holding chunks i and 2P-1-i (outer index (i*bsz + b)*2 + half); o decodes to
 // (i, b, query half), the launch's KV half is zz_kh, positions are chunk * np.
+// split_np > 0 (Ulysses attention read and written in place in the sequence-
+// sharded layout [P][B][split_np][H][d]): the launch decodes like the head-
+// sharded path with one outer index per batch (ring_p = 1, bsz = n_outer = B)
+// over global positions, and every token coordinate passes through split_pos
+// (ptx.cuh): position pos of batch b is token pos % split_np of outer index
+// (pos / split_np) * split_b + b.  split_np must be a multiple of 128, so that
+// no 128-row tile straddles two shards.
 struct FwdParams {
     Tensor4 q, k, v;
     int d;
@@ -51,6 +58,7 @@ struct FwdParams {
     int ring_i0, ring_t, ring_p, bsz, np;
     int kv_gathered;
     int zigzag, zz_kh;
+    int split_np, split_b;
     int causal;
     float scale;
     // epilogue: o_bf16 (bf16, strides as q) or o_f32 (float32); one is null
@@ -88,6 +96,9 @@ struct BwdParams {
     // zigzag ring (as FwdParams): zz_kh is the launch's KV half; zz_qh >= 0 fixes the query half
     // (the outer index is then (rank, batch) only), -1 takes it from the outer index
     int zigzag, zz_kh, zz_qh;
+    // in place in the sequence-sharded layout (as FwdParams): q, k, v, o, dout, lse and the results;
+    // the workspace rows are indexed by (batch, head, global position)
+    int split_np, split_b;
     float scale;
     int* status;
 };

@@ -287,6 +287,18 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
+// Attention read and written in place in the sequence-sharded layout
+// [P][B][np][H][d]: global position pos of batch b sits at token pos % np of
+// outer index (pos / np) * nb + b.  np == 0 leaves (pos, outer) unchanged.
+struct TokOuter {
+    int tok, outer;
+};
+__device__ __forceinline__ TokOuter split_pos(int pos, int outer, int np, int nb) {
+    if (np == 0) return {pos, outer};
+    const int shard = pos / np;
+    return {pos - shard * np, shard * nb + outer};
+}
+
 // Two floats -> packed bf16x2 (round to nearest even); lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;

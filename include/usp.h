@@ -24,8 +24,11 @@
  *   logical          [B][H][N][d]
  *   sequence-sharded [P][B][N/P][H][d]   rank p holds tokens [p*N/P, (p+1)*N/P)
  *   head-sharded     [P][B][H/P][N][d]   rank r holds heads  [r*H/P, (r+1)*H/P)
+ *   hybrid (2-D)     [P][B][H/Pu][N/Pr][d] rank g*Pu + u holds heads
+ *                    [u*H/Pu, (u+1)*H/Pu) of token chunk g (P = Pu * Pr)
  *   LSE (head-sharded attention)    float32 [P][B][Hq/P][N]
- *   LSE (sequence-sharded ring)     float32 [P][B][N/P][Hq]
+ *   LSE (sequence-sharded ring, all-gather, fused) float32 [P][B][N/P][Hq]
+ *   LSE (hybrid)                    float32 [P][B][Hq/Pu][N/Pr]
  * H is Hq for Q, O, dO, dQ and Hkv for K, V, dK, dV.  Query head h attends
  * with KV head h / (Hq/Hkv) (contiguous groups); each rank's query heads then
  * use only that rank's KV heads.
@@ -278,6 +281,76 @@ usp_status usp_zigzag_attn_fwd(const usp_problem* p, const void* q, const void* 
 usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
                                const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                                size_t ws_bytes, usp_stream stream);
+
+/* ---- Ulysses attention with the all-to-all fused into the kernels ("Million-
+ * Token-Kontexte im Training", bytewire.ai, "Ulysses: Die Sequenz als
+ * Verteilungseinheit": the exchange that gives each rank the whole sequence
+ * for its heads).  The attention kernels read Q, K, V and dO and write O, LSE,
+ * dQ, dK and dV in place in the sequence-sharded layout: every tile load and
+ * every result row addresses token n of a head as row n mod (N/P) of shard
+ * n div (N/P), so no remap runs and no head-sharded copy exists.  Results are
+ * those of usp_a2a_seq2head -> usp_attn_fwd / usp_attn_bwd -> usp_a2a_head2seq,
+ * bit for bit (the same per-head work, tile for tile); only the LSE layout
+ * differs: float32 [P][B][N/P][Hq], as in ring mode.
+ * Preconditions as usp_attn_fwd (Hq % P = Hkv % P = 0, dtype BF16, d in
+ * {64, 128}) plus (N/P) % 128 == 0: a 128-row tile never straddles two shards
+ * (USP_ERR_UNSUPPORTED otherwise). */
+usp_status usp_fused_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
+                              float* lse, usp_stream stream);
+
+/* Bytes of workspace usp_fused_attn_bwd needs (equal to
+ * usp_attn_bwd_workspace_size); 0 for an invalid problem. */
+size_t usp_fused_attn_bwd_workspace_size(const usp_problem* p);
+
+/* Backward of usp_fused_attn_fwd: q, k, v, o, dout, dq, dk, dv sequence-
+ * sharded, lse as the forward wrote it.  ws: at least
+ * usp_fused_attn_bwd_workspace_size(p) bytes, 256-byte aligned. */
+usp_status usp_fused_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                              size_t ws_bytes, usp_stream stream);
+
+/* ---- 2-D (hybrid) sequence parallelism: Ulysses inside groups of Pu ranks,
+ * ring attention across the Pr = P/Pu groups (the pages name hybrid
+ * strategies -- bytewire.ai, "Praktische Implikationen fuer den Einsatz" --
+ * and both exchanges: the all-to-all, and the ring of "Context Parallelism",
+ * ultralytics.com, "So funktioniert Kontextparallelitaet").
+ * Group g holds the contiguous token chunk g of Nc = N/Pr tokens (its ranks
+ * g*Pu .. g*Pu + Pu - 1 hold the chunk's Pu shards of N/P tokens).  The
+ * all-to-all inside the group gives rank g*Pu + u the heads u*H/Pu ..
+ * (u+1)*H/Pu - 1 of the chunk: the hybrid layout [P][B][H/Pu][Nc][d], LSE
+ * float32 [P][B][Hq/Pu][Nc].  Pu = P is the Ulysses layout (Pr = 1), Pu = 1
+ * per-rank head-major shards of the ring.
+ * Every hybrid call: Pu >= 1, P % Pu == 0, Hq % Pu == 0, Hkv % Pu == 0 (else
+ * USP_ERR_INVALID_ARG), plus the usp_problem checks without the head split. */
+
+/* Sequence-sharded [P][B][N/P][Hx][d] -> hybrid layout (one Ulysses remap of
+ * Nc tokens over Pu ranks per group), and back.  Bit copies, any dtype,
+ * d * element size in {64, 128, 256, 512} bytes; src and dst must not
+ * overlap. */
+usp_status usp_hybrid_seq2head(const usp_problem* p, int Pu, int Hx, const void* src, void* dst, usp_stream stream);
+usp_status usp_hybrid_head2seq(const usp_problem* p, int Pu, int Hx, const void* src, void* dst, usp_stream stream);
+
+/* Bytes of workspace usp_hybrid_attn_fwd needs (float32 running and partial
+ * outputs and partial LSE, as usp_ring_workspace_size) and usp_hybrid_attn_bwd
+ * needs (40 bytes per padded query row of every rank and local head, float32
+ * dQ, dK, dV accumulators); 0 for an invalid problem. */
+size_t usp_hybrid_workspace_size(const usp_problem* p, int Pu);
+size_t usp_hybrid_bwd_workspace_size(const usp_problem* p, int Pu);
+
+/* Hybrid forward on hybrid-layout q, k, v: at ring step t = 0..Pr-1 the ranks
+ * of group i attend their heads of chunk i to the same heads' KV of chunk
+ * j = (i - t) mod Pr (skipped when j > i under the causal mask), each partial
+ * merged by log-sum-exp as usp_ring_attn_fwd does; o (bf16) and lse in the
+ * hybrid layout.  dtype BF16, d in {64, 128}; ws 256-byte aligned. */
+usp_status usp_hybrid_attn_fwd(const usp_problem* p, int Pu, const void* q, const void* k, const void* v, void* o,
+                               float* lse, void* ws, size_t ws_bytes, usp_stream stream);
+
+/* Hybrid backward: usp_ring_attn_bwd's schedule over the groups (dK, dV
+ * travel with the KV chunk, dQ stays), float32, rounded once to bf16; every
+ * tensor in the hybrid layout, lse as the forward wrote it. */
+usp_status usp_hybrid_attn_bwd(const usp_problem* p, int Pu, const void* q, const void* k, const void* v,
+                               const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* ws, size_t ws_bytes, usp_stream stream);
 
 /* Exact merge of two partial attentions over disjoint key sets, float32
  * (the merge step of ring attention):

@@ -49,6 +49,31 @@ def from_head(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(np.swapaxes(x, 0, 1).reshape(B, P * Hl, *rest))
 
 
+def to_hybrid(x: np.ndarray, P: int, Pu: int) -> np.ndarray:
+    """logical [B][H][N][d] -> 2-D layout [P][B][H/Pu][N/Pr][d] (Pr = P/Pu; rank g*Pu + u holds
+    heads u*H/Pu .. of token chunk g) (copy)."""
+    B, H, N, d = x.shape
+    Pr = P // Pu
+    y = x.reshape(B, Pu, H // Pu, Pr, N // Pr, d).transpose(3, 1, 0, 2, 4, 5)
+    return np.ascontiguousarray(y.reshape(P, B, H // Pu, N // Pr, d))
+
+
+def from_hybrid(x: np.ndarray, Pu: int) -> np.ndarray:
+    """2-D layout [P][B][H/Pu][N/Pr](...) (tensor or LSE) -> logical [B][H][N](...) (copy)."""
+    P, B, Hl, Nc = x.shape[:4]
+    rest = x.shape[4:]
+    Pr = P // Pu
+    y = x.reshape(Pr, Pu, B, Hl, Nc, *rest)
+    y = np.moveaxis(y, [2, 1, 3, 0, 4], [0, 1, 2, 3, 4])
+    return np.ascontiguousarray(y.reshape(B, Pu * Hl, Pr * Nc, *rest))
+
+
+def lse_from_seq(x: np.ndarray) -> np.ndarray:
+    """sequence-sharded LSE [P][B][N/P][Hq] -> logical [B][Hq][N] (copy)."""
+    P, B, Np, H = x.shape
+    return np.ascontiguousarray(x.transpose(1, 3, 0, 2).reshape(B, H, P * Np))
+
+
 def f64(x: np.ndarray) -> np.ndarray:
     if x.dtype == np.uint16:
         return synth.bf16_to_f32(x).astype(np.float64)

@@ -140,6 +140,11 @@ def test_empty_problems_enqueue_nothing(lib):
         usp.usp_zigzag_attn_fwd(p, 0, 0, 0, 0, 0, 0, 0)
         usp.usp_zigzag_attn_bwd(p, *([0] * 9), 0, 0)
         usp.usp_zigzag_shard(p, 4, 0, 0)
+        usp.usp_fused_attn_fwd(p, 0, 0, 0, 0, 0)
+        usp.usp_fused_attn_bwd(p, *([0] * 9), 0, 0)
+        usp.usp_hybrid_seq2head(p, 2, 4, 0, 0)
+        usp.usp_hybrid_attn_fwd(p, 2, 0, 0, 0, 0, 0, 0, 0)
+        usp.usp_hybrid_attn_bwd(p, 2, *([0] * 9), 0, 0)
     usp.usp_ring_merge(0, 64, 0, 0, 0, 0, 0, 0)
 
 
@@ -213,3 +218,73 @@ def test_zigzag_argument_errors(lib):
     with pytest.raises(usp.UspError) as e:
         usp.usp_zigzag_attn_bwd(p, *([FAKE] * 9), FAKE + 64, bws)   # workspace must be 256-byte aligned
     assert e.value.status == _lib.USP_ERR_MISALIGNED
+
+
+def test_fused_argument_errors(lib):
+    p = _p()                                                   # N/P = 128: one tile per shard
+    bws = usp.usp_fused_attn_bwd_workspace_size(p)
+    assert bws == usp.usp_attn_bwd_workspace_size(p) == 40 * p.B * p.Hq * p.N
+    for kw, code in ((dict(N=200), _lib.USP_ERR_UNSUPPORTED),  # shards of 100 tokens: tiles would straddle
+                     (dict(N=384), _lib.USP_ERR_UNSUPPORTED),  # shards of 192 tokens
+                     (dict(Hq=3, Hkv=3), _lib.USP_ERR_INVALID_ARG),   # heads are split over the ranks
+                     (dict(dtype="f32"), _lib.USP_ERR_UNSUPPORTED),
+                     (dict(d=32), _lib.USP_ERR_UNSUPPORTED)):
+        with pytest.raises(usp.UspError) as e:
+            usp.usp_fused_attn_fwd(_p(**kw), FAKE, FAKE, FAKE, FAKE, FAKE)
+        assert e.value.status == code, kw
+        with pytest.raises(usp.UspError) as e:
+            usp.usp_fused_attn_bwd(_p(**kw), *([FAKE] * 9), FAKE, 1 << 40)
+        assert e.value.status == code, kw
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_fused_attn_fwd(p, FAKE, FAKE, FAKE + 8, FAKE, FAKE)   # v not 16-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_fused_attn_bwd(p, *([FAKE] * 9), FAKE, bws - 256)
+    assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_fused_attn_bwd(p, *([FAKE] * 9), FAKE + 16, bws)       # workspace must be 256-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+
+
+def test_hybrid_argument_errors(lib):
+    p = _p(P=4, N=1024, Hq=8, Hkv=4, d=128)
+    for Pu in (0, -2, 3, 8):                                   # Pu >= 1 dividing P
+        assert usp.usp_hybrid_workspace_size(p, Pu) == 0
+        assert usp.usp_hybrid_bwd_workspace_size(p, Pu) == 0
+        with pytest.raises(usp.UspError) as e:
+            usp.usp_hybrid_seq2head(p, Pu, 8, FAKE, FAKE * 64)
+        assert e.value.status == _lib.USP_ERR_INVALID_ARG
+        with pytest.raises(usp.UspError) as e:
+            usp.usp_hybrid_attn_fwd(p, Pu, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40)
+        assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    with pytest.raises(usp.UspError) as e:                     # Hkv % Pu
+        usp.usp_hybrid_attn_fwd(_p(P=4, N=1024, Hq=8, Hkv=2, d=128), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40)
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    # heads split over Pu only: Hq = 8 on P = 6 ranks is a valid 2 x 3 problem
+    assert usp.usp_hybrid_workspace_size(_p(P=6, N=1536, Hq=8, Hkv=4, d=128), 2) > 0
+    for Pu in (1, 2, 4):
+        Pr, Nc = 4 // Pu, 1024 // (4 // Pu)
+        ws = usp.usp_hybrid_workspace_size(p, Pu)
+        assert ws == usp.usp_ring_workspace_size(p)            # float32 running and partial O, partial LSE
+        bws = usp.usp_hybrid_bwd_workspace_size(p, Pu)
+        # 40 bytes per padded query row of every (rank, local head), float32 dQ, dK, dV accumulators
+        assert bws == 40 * 4 * (8 // Pu) * ((Nc + 127) // 128 * 128) + 4 * 1024 * 128 * (8 + 2 * 4)
+        with pytest.raises(usp.UspError) as e:
+            usp.usp_hybrid_attn_fwd(p, Pu, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 256)
+        assert e.value.status == _lib.USP_ERR_WORKSPACE
+        with pytest.raises(usp.UspError) as e:
+            usp.usp_hybrid_attn_bwd(p, Pu, *([FAKE] * 9), FAKE, bws - 256)
+        assert e.value.status == _lib.USP_ERR_WORKSPACE
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_hybrid_seq2head(p, 2, 8, FAKE, FAKE + 256)       # overlapping buffers
+    assert e.value.status == _lib.USP_ERR_INVALID_ARG
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_hybrid_seq2head(_p(P=4, N=1024, Hq=8, Hkv=4, d=24), 2, 8, FAKE, FAKE * 64)   # 48-byte rows
+    assert e.value.status == _lib.USP_ERR_UNSUPPORTED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_hybrid_attn_fwd(_p(P=4, N=1024, Hq=8, Hkv=4, d=128, dtype="f32"), 2, *([FAKE] * 6), 1 << 40)
+    assert e.value.status == _lib.USP_ERR_UNSUPPORTED
+    with pytest.raises(usp.UspError) as e:
+        usp.usp_hybrid_attn_bwd(p, 2, *([FAKE] * 9), FAKE + 64, 1 << 40)   # workspace must be 256-byte aligned
+    assert e.value.status == _lib.USP_ERR_MISALIGNED
+

@@ -4,8 +4,8 @@ import numpy as np
 import pytest
 
 from tests.helpers import (TOL_BF16_GRAD_RELFRO, TOL_BF16_O_MAXABS, TOL_BF16_O_RELFRO, TOL_F32_MAXABS, TOL_LSE_BF16,
-                           TOL_LSE_F32, f64, from_head, from_seq, gen, max_abs, rel_fro, to_dev, to_head, to_host,
-                           to_seq)
+                           TOL_LSE_F32, f64, from_head, from_hybrid, from_seq, gen, lse_from_seq, max_abs, rel_fro,
+                           to_dev, to_head, to_host, to_hybrid, to_seq)
 
 pytestmark = pytest.mark.gpu
 
@@ -326,3 +326,120 @@ def test_zigzag_ring_fwd_bwd(usp, orc, B, H, Hkv, N, d, P, causal):
     ref_dq, ref_dk, ref_dv, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
     _check_grads(out, ref_dq, ref_dk, ref_dv)
     _status_ok(usp)
+
+
+# ---------------------------------------------------------------- all-to-all fused into attention
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,P,causal", [
+    (1, 8, 2, 1024, 128, 4, True),     # GQA, four shards of 256 tokens
+    (2, 4, 4, 512, 64, 2, True),       # two sequences
+    (1, 4, 2, 768, 128, 2, False),     # full attention, shards of 384 tokens
+    (1, 2, 2, 256, 64, 1, True),       # one rank
+    (1, 8, 8, 1024, 128, 8, True),     # eight shards of one 128-row tile each
+    (1, 6, 3, 384, 64, 3, True)])      # three shards: the last 256-row block's second tile is past N
+def test_fused_equals_remapped_bitwise(usp, B, Hq, Hkv, N, d, P, causal):
+    """Attention reading and writing the sequence-sharded layout in place gives the remapped
+    path's O, LSE, dQ, dK and dV bit for bit (the same per-head work, tile for tile)."""
+    import torch
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P, causal=causal)
+    q, k, v, dO = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2), gen((B, Hq, N, d), 3)
+    qs, ks, vs, dos = (to_dev(to_seq(x, P)) for x in (q, k, v, dO))
+    o_r, saved = usp.ulysses_attention_fwd(p, qs, ks, vs)
+    dq_r, dk_r, dv_r = usp.ulysses_attention_bwd(p, saved, dos)
+    o, lse = usp.fused_attention_fwd(p, qs, ks, vs)
+    dq, dk, dv = usp.fused_attention_bwd(p, qs, ks, vs, o, lse, dos)
+    torch.cuda.synchronize()
+    for got, want in ((o, o_r), (dq, dq_r), (dk, dk_r), (dv, dv_r)):
+        assert to_host(got).tobytes() == to_host(want).tobytes()
+    assert lse_from_seq(to_host(lse)).tobytes() == from_head(to_host(saved["lse"])).tobytes()
+    _status_ok(usp)
+
+
+def test_fused_against_oracle_mean_square_loss(usp, orc):
+    """The fused path against the float64 oracle on its own: loss mean(out^2), GQA, four shards."""
+    import torch
+    B, Hq, Hkv, N, d, P = 1, 8, 2, 2048, 128, 4
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P)
+    q, k, v = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2)
+    qs, ks, vs = (to_dev(to_seq(x, P)) for x in (q, k, v))
+    o, lse = usp.fused_attention_fwd(p, qs, ks, vs)
+    do_seq = (2.0 * o.float() / o.numel()).to(torch.bfloat16)
+    dq, dk, dv = usp.fused_attention_bwd(p, qs, ks, vs, o, lse, do_seq)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=True)
+    _check_fwd(from_seq(to_host(o)), lse_from_seq(to_host(lse)), o_ref, lse_ref)
+    dO_ref = (2.0 * o_ref / o_ref.size).astype(np.float32)
+    ref_dq, ref_dk, ref_dv, _, _ = orc.attn_bwd_full(q, k, v, dO_ref, causal=True)
+    out = dict(dq=from_seq(to_host(dq)), dk=from_seq(to_host(dk)), dv=from_seq(to_host(dv)))
+    _check_grads(out, ref_dq, ref_dk, ref_dv)
+    _status_ok(usp)
+
+
+# ---------------------------------------------------------------- 2-D (hybrid) Ulysses x ring
+@pytest.mark.parametrize("dtype,B,H,N,d,P,Pu", [
+    ("bf16", 2, 8, 1200, 128, 4, 2), ("f32", 1, 6, 768, 64, 6, 3), ("bf16", 1, 4, 512, 64, 4, 1),
+    ("bf16", 1, 8, 512, 128, 4, 4)])
+def test_hybrid_remap_bit_exact(usp, orc, dtype, B, H, N, d, P, Pu):
+    """The all-to-all inside each ring group: the oracle's Ulysses map on the group's shards."""
+    import torch
+    p = usp.Problem(B=B, Hq=H, Hkv=H, N=N, d=d, P=P, dtype=dtype)
+    x = gen((B, H, N, d), 4, dtype)
+    seq = to_seq(x, P)
+    src = to_dev(seq, dtype)
+    hyb = torch.empty(p.hybrid_shape(H, Pu), dtype=p.torch_dtype, device="cuda")
+    back = torch.empty_like(src)
+    usp.usp_hybrid_seq2head(p, Pu, H, src, hyb)
+    usp.usp_hybrid_head2seq(p, Pu, H, hyb, back)
+    _sync()
+    want = np.concatenate([orc.seq2head(seq[g * Pu:(g + 1) * Pu]) for g in range(P // Pu)])
+    assert to_host(hyb).tobytes() == want.tobytes()
+    assert to_host(hyb).tobytes() == to_hybrid(x, P, Pu).tobytes()
+    assert to_host(back).tobytes() == seq.tobytes()
+    _status_ok(usp)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,P,Pu,causal", [
+    (1, 8, 4, 2048, 128, 4, 2, True),     # two ring groups of two Ulysses ranks
+    (2, 4, 2, 1200, 64, 4, 2, True),      # two sequences, GQA, chunks of 600 tokens (ragged tiles)
+    (1, 8, 8, 1536, 128, 6, 2, True),     # three ring groups
+    (1, 8, 2, 1024, 128, 4, 2, False)])   # full attention, GQA group of 4
+def test_hybrid_fwd_bwd(usp, orc, B, Hq, Hkv, N, d, P, Pu, causal):
+    """2-D sequence parallelism (forward and backward) against the oracle."""
+    import torch
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P, causal=causal)
+    q, k, v, dO = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2), gen((B, Hq, N, d), 3)
+    qs, ks, vs, dos = (to_dev(to_seq(x, P)) for x in (q, k, v, dO))
+    o, saved = usp.hybrid_attention_fwd(p, Pu, qs, ks, vs)
+    dq, dk, dv = usp.hybrid_attention_bwd(p, Pu, saved, dos)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = orc.attn_rows(q, k, v, causal=causal)
+    _check_fwd(from_seq(to_host(o)), from_hybrid(to_host(saved["lse"]), Pu), o_ref, lse_ref)
+    ref_dq, ref_dk, ref_dv, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
+    out = dict(dq=from_seq(to_host(dq)), dk=from_seq(to_host(dk)), dv=from_seq(to_host(dv)))
+    _check_grads(out, ref_dq, ref_dk, ref_dv)
+    _status_ok(usp)
+
+
+def test_hybrid_reduces_to_ulysses_and_ring_bitwise(usp):
+    """Pu = P is one ring group: the Ulysses path; Pu = 1 is the ring.  Both bit for bit."""
+    import torch
+    B, Hq, Hkv, N, d, P = 1, 8, 4, 1024, 128, 4
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P)
+    q, k, v, dO = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2), gen((B, Hq, N, d), 3)
+    qs, ks, vs, dos = (to_dev(to_seq(x, P)) for x in (q, k, v, dO))
+    o_u, saved_u = usp.ulysses_attention_fwd(p, qs, ks, vs)
+    g_u = usp.ulysses_attention_bwd(p, saved_u, dos)
+    o_h, saved_h = usp.hybrid_attention_fwd(p, P, qs, ks, vs)
+    g_h = usp.hybrid_attention_bwd(p, P, saved_h, dos)
+    o_r, lse_r = usp.ring_attention_fwd(p, qs, ks, vs)
+    g_r = usp.ring_attention_bwd(p, qs, ks, vs, o_r, lse_r, dos)
+    o_1, saved_1 = usp.hybrid_attention_fwd(p, 1, qs, ks, vs)
+    g_1 = usp.hybrid_attention_bwd(p, 1, saved_1, dos)
+    torch.cuda.synchronize()
+    for got, want in zip((o_h, *g_h), (o_u, *g_u)):
+        assert to_host(got).tobytes() == to_host(want).tobytes()
+    assert to_host(saved_h["lse"]).tobytes() == to_host(saved_u["lse"]).tobytes()
+    for got, want in zip((o_1, *g_1), (o_r, *g_r)):
+        assert to_host(got).tobytes() == to_host(want).tobytes()
+    assert from_hybrid(to_host(saved_1["lse"]), 1).tobytes() == lse_from_seq(to_host(lse_r)).tobytes()
+    _status_ok(usp)
+

@@ -116,6 +116,27 @@ def test_seq2head_matches_head_split(orc, B, H, N, d, P, dtype):
     assert np.array_equal(orc.seq2head(orc.head2seq(y)), y)
 
 
+@pytest.mark.parametrize("B,H,N,d,P,Pu", [(2, 8, 24, 3, 4, 2), (1, 6, 36, 2, 6, 3), (1, 4, 16, 1, 4, 1),
+                                          (2, 4, 16, 2, 4, 4)])
+def test_group_seq2head_gives_the_2d_layout(orc, B, H, N, d, P, Pu):
+    """2-D sequence parallelism: the all-to-all inside each ring group of Pu consecutive ranks
+    (the oracle's Ulysses map on that group's shards) leaves rank g*Pu + u with heads
+    u*H/Pu .. of token chunk g -- element by element."""
+    from tests.helpers import from_hybrid, to_hybrid
+    x = _coded((B, H, N, d), np.float32)
+    seq = orc.shard_seq(x, P)
+    Pr, Nc, Hl = P // Pu, N // (P // Pu), H // Pu
+    hyb = np.concatenate([orc.seq2head(seq[g * Pu:(g + 1) * Pu]) for g in range(Pr)])
+    assert hyb.shape == (P, B, Hl, Nc, d)
+    for g in range(Pr):
+        for u in range(Pu):
+            for b in range(B):
+                for hl in range(Hl):
+                    assert np.array_equal(hyb[g * Pu + u, b, hl], x[b, u * Hl + hl, g * Nc:(g + 1) * Nc])
+    assert np.array_equal(hyb, to_hybrid(x, P, Pu))
+    assert np.array_equal(from_hybrid(hyb, Pu), x)
+
+
 def test_seq2head_is_a_permutation(orc):
     B, H, N, d, P = 2, 8, 16, 3, 4
     x = _coded((P, B, N // P, H, d))
