@@ -57,9 +57,9 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
 # sources they were taken on: a changed kernel reports null until re-measured.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (2932230912 + 1159816192, "644d5a0be1fde1cf", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (9136004864 + 526604800, "da0ad8f5c69e2d93", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (4428167680 + 1050199552, "da0ad8f5c69e2d93", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (2924220160 + 1160072448, "060417e63914f8b5", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (9132134144 + 526144000, "484bd2383c370539", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (4461772800 + 1050943488, "484bd2383c370539", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 
@@ -575,9 +575,10 @@ def bench_allgather(usp, torch, dev, peaks, w):
 
 
 def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
-    """Two variants of the step on its workload, one untimed and one timed pass each:
-    the all-to-all fused into the attention kernels (no remap launches), and 2-D sequence
-    parallelism (Ulysses inside groups of Pu = P/2 ranks, ring across the 2 groups)."""
+    """Two variants of the step on its workload: the all-to-all fused into the attention kernels
+    (no remap launches; two timed passes, each after a pass of the remapped step), and 2-D
+    sequence parallelism (Ulysses inside groups of Pu = P/2 ranks, ring across the 2 groups; one
+    untimed and one timed pass)."""
     import numpy as np
     import synth
     p = usp.Problem(**w, causal=True)
@@ -598,32 +599,66 @@ def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
     f = fwd_flops(w)
     e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
 
-    # ---- fused: sequence-sharded in, sequence-sharded out, three attention launches per pass
+    # ---- fused: sequence-sharded in, sequence-sharded out, four launches per pass. The remapped
+    # step (remaps, attention, remaps back, on the same inputs) is timed alternately with it, so
+    # that both see the same clock and power state.
     lse = torch.empty(p.lse_seq_shape(), dtype=torch.float32, device=dev)
     ws = torch.empty(usp.usp_fused_attn_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
-    for timed in (False, True):
-        if timed:
-            usp.usp_trace_reset()
-            usp.usp_trace_enable(True)
+    qh = torch.empty(p.head_shape(Hq), dtype=torch.bfloat16, device=dev)
+    kh, vh = (torch.empty(p.head_shape(Hkv), dtype=torch.bfloat16, device=dev) for _ in range(2))
+    oh, doh, dqh = (torch.empty_like(qh) for _ in range(3))
+    dkh, dvh = torch.empty_like(kh), torch.empty_like(vh)
+    lse_h = torch.empty(p.lse_head_shape(), dtype=torch.float32, device=dev)
+
+    def fused_pass():
         e0.record(s)
         usp.usp_fused_attn_fwd(p, q, k, v, o, lse, sh)
         e1.record(s)
         usp.usp_fused_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, None, sh)
         e2.record(s)
         torch.cuda.synchronize()
-    usp.usp_trace_enable(False)
+        return e0.elapsed_time(e1), e1.elapsed_time(e2)
+
+    def remapped_pass():
+        e0.record(s)
+        usp.usp_a2a_seq2head(p, Hq, q, qh, sh)
+        usp.usp_a2a_seq2head(p, Hkv, k, kh, sh)
+        usp.usp_a2a_seq2head(p, Hkv, v, vh, sh)
+        usp.usp_attn_fwd(p, qh, kh, vh, oh, lse_h, sh)
+        usp.usp_a2a_head2seq(p, Hq, oh, o, sh)
+        usp.usp_a2a_seq2head(p, Hq, dout, doh, sh)
+        usp.usp_attn_bwd(p, qh, kh, vh, oh, lse_h, doh, dqh, dkh, dvh, ws, None, sh)
+        usp.usp_a2a_head2seq(p, Hq, dqh, dq, sh)
+        usp.usp_a2a_head2seq(p, Hkv, dkh, dk, sh)
+        usp.usp_a2a_head2seq(p, Hkv, dvh, dv, sh)
+        e2.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e2)
+
+    fused_pass()
+    fwd_ms, bwd_ms, remapped_ms = [], [], []
+    usp.usp_trace_reset()
+    for _ in range(2):
+        remapped_ms.append(remapped_pass())
+        usp.usp_trace_enable(True)
+        a, b = fused_pass()
+        usp.usp_trace_enable(False)
+        fwd_ms.append(a)
+        bwd_ms.append(b)
     ftrace = usp.usp_trace_report()
-    ffwd, fbwd = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    ffwd, fbwd, rms = sum(fwd_ms) / 2, sum(bwd_ms) / 2, sum(remapped_ms) / 2
     ok = usp.usp_device_status(sh) == 0
-    del lse, ws
+    del lse, ws, qh, kh, vh, oh, doh, dqh, dkh, dvh, lse_h
     torch.cuda.empty_cache()
-    fused = {"workload": f"{WORKLOAD_NAME}: Ulysses step with the all-to-all fused into the kernels "
+    fused = {"workload": "the step's workload with the all-to-all fused into the attention kernels "
                          "(sequence-sharded operands read and written in place; no remap launches)",
              "fwd_ms": ffwd, "bwd_ms": fbwd, "ms_per_step": ffwd + fbwd,
              "step_TFLOPs": 3.5 * f / ((ffwd + fbwd) * 1e-3) / 1e12,
              "frac_sustained": 3.5 * f / ((ffwd + fbwd) * 1e-3) / 1e12 / peaks["bf16_sus"],
-             "kernels_ms": {k_: v_[1] for k_, v_ in ftrace.items()},
-             "launches_per_step": sum(v_[0] for v_ in ftrace.values()), "status_ok": ok}
+             "remapped_ms_per_step_alternating": rms,
+             "kernels_ms_per_step": {k_: v_[1] / v_[0] for k_, v_ in ftrace.items()},
+             "launches_per_step": sum(v_[0] for v_ in ftrace.values()) // 2, "status_ok": ok,
+             "timing": "mean of 2 passes, each after one pass of the remapped step on the same inputs"}
 
     # ---- 2-D: all-to-all inside 2 groups of P/2 ranks, ring over the 2 groups, all-to-all back
     Pu = max(1, P // 2)
@@ -658,8 +693,8 @@ def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
     ok = usp.usp_device_status(sh) == 0
     del q, k, v, dout, o, dq, dk, dv, hq, hk, hv, hdk, hdv, ho, hdo, hdq, hlse, hws
     torch.cuda.empty_cache()
-    hybrid = {"workload": f"{WORKLOAD_NAME}: 2-D sequence parallelism, Pu={Pu} Ulysses ranks x Pr={P // Pu} ring "
-                          "groups (all-to-all inside groups, ring across them, all-to-all back)",
+    hybrid = {"workload": f"the step's workload under 2-D sequence parallelism, Pu={Pu} Ulysses ranks x "
+                          f"Pr={P // Pu} ring groups (all-to-all inside groups, ring across them, all-to-all back)",
               "Pu": Pu, "Pr": P // Pu, "fwd_ms": hfwd, "bwd_ms": hbwd, "ms_per_step": hfwd + hbwd,
               "step_TFLOPs": 3.5 * f / ((hfwd + hbwd) * 1e-3) / 1e12,
               "kernels_ms": {k_: v_[1] for k_, v_ in htrace.items()},

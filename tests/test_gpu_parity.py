@@ -330,7 +330,8 @@ def test_zigzag_ring_fwd_bwd(usp, orc, B, H, Hkv, N, d, P, causal):
 
 # ---------------------------------------------------------------- all-to-all fused into attention
 @pytest.mark.parametrize("B,Hq,Hkv,N,d,P,causal", [
-    (1, 8, 2, 1024, 128, 4, True),     # GQA, four shards of 256 tokens
+    (1, 8, 4, 1024, 128, 4, True),     # GQA, four shards of 256 tokens
+    (1, 16, 4, 512, 128, 4, True),     # GQA group of 4, shards of one tile
     (2, 4, 4, 512, 64, 2, True),       # two sequences
     (1, 4, 2, 768, 128, 2, False),     # full attention, shards of 384 tokens
     (1, 2, 2, 256, 64, 1, True),       # one rank
@@ -357,7 +358,7 @@ def test_fused_equals_remapped_bitwise(usp, B, Hq, Hkv, N, d, P, causal):
 def test_fused_against_oracle_mean_square_loss(usp, orc):
     """The fused path against the float64 oracle on its own: loss mean(out^2), GQA, four shards."""
     import torch
-    B, Hq, Hkv, N, d, P = 1, 8, 2, 2048, 128, 4
+    B, Hq, Hkv, N, d, P = 1, 8, 4, 2048, 128, 4
     p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P)
     q, k, v = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2)
     qs, ks, vs = (to_dev(to_seq(x, P)) for x in (q, k, v))
