@@ -7,6 +7,8 @@ oracle cannot afford every row) and against properties that hold at any size:
     (their rows i >= j are few enough for the oracle), plus
     sum_j dK_j = 0 (softmax shift invariance) and sum_j dV_j = sum_i dO_i,
     within the bound the per-element tolerance implies for a sum;
+  - the all-to-all fused into the kernels (sequence-sharded operands read and
+    written in place) gives the remapped path's O, LSE and gradients bit for bit;
   - ring attention equals one full-sequence pass and the oracle's rows;
   - ring backward gradients against the oracle on sampled dQ rows and tail
     dK/dV rows, plus the same sum identities.
@@ -65,6 +67,17 @@ def test_ulysses_long_context(usp, orc, B, Hq, Hkv, N, d, P):
     dq_s, dk_s, dv_s = usp.ulysses_attention_bwd(p, saved, dos)
     torch.cuda.synchronize()
     assert usp.usp_device_status() == 0
+
+    # the fused path at full size: the same bits, no remap
+    o_f, lse_f = usp.fused_attention_fwd(p, qs, ks, vs)
+    grads_f = usp.fused_attention_bwd(p, qs, ks, vs, o_f, lse_f, dos)
+    torch.cuda.synchronize()
+    assert usp.usp_device_status() == 0
+    for got, want in zip((o_f, *grads_f), (o_seq, dq_s, dk_s, dv_s)):
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    lse_u = saved["lse"].permute(1, 0, 2, 3).reshape(B, Hq, N)
+    assert torch.equal(lse_f.permute(1, 3, 0, 2).reshape(B, Hq, N).view(torch.int32), lse_u.view(torch.int32))
+    del o_f, lse_f, grads_f, lse_u
 
     # all-to-all: the oracle's index map, bit for bit
     assert to_host(saved["k"]).tobytes() == orc.seq2head(to_host(ks)).tobytes()
