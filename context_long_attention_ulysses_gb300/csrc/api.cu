@@ -982,13 +982,13 @@ static usp_status hybrid_a2a(int dir, const usp_problem* p, int Pu, int Hx, cons
     const int Pr = p->P / Pu, Nc = p->N / Pr;
     const size_t blk = bytes / Pr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return cuda_status(traced(dir == 0 ? "hybrid_seq2head" : "hybrid_head2seq", s, [&] {
-        for (int g = 0; g < Pr; ++g) {
-            cudaError_t e = launch_remap(dir, sb + g * blk, tb + g * blk, p->B, Hx, Nc, Pu, row_bytes, s);
-            if (e != cudaSuccess) return e;
-        }
-        return cudaSuccess;
-    }));
+    for (int g = 0; g < Pr; ++g) {
+        cudaError_t e = traced(dir == 0 ? "hybrid_seq2head" : "hybrid_head2seq", s, [&] {
+            return launch_remap(dir, sb + g * blk, tb + g * blk, p->B, Hx, Nc, Pu, row_bytes, s);
+        });
+        if (e != cudaSuccess) return USP_ERR_CUDA;
+    }
+    return USP_OK;
 }
 
 usp_status usp_hybrid_seq2head(const usp_problem* p, int Pu, int Hx, const void* src, void* dst, usp_stream stream) {
