@@ -320,6 +320,60 @@ usp_status usp_ring_merge(int64_t rows, int d, const float* o_a, const float* ls
         traced("ring_merge", s, [&] { return launch_lse_merge(rows, d, o_a, lse_a, o_b, lse_b, o, lse, s); }));
 }
 
+// The ring schedule over n_groups ring members, for a forward whose tensors and decode are set
+// (ring_p = n_groups; outer index = member * per_member + the index within the member).  Step t
+// attends member i's queries to member (i - t) mod n_groups's keys -- under the causal mask only
+// members i >= t, the rest see none of those keys -- and merges each partial into the running
+// float32 output (rows in member-major order, rows_per_member each) by log-sum-exp.  The final
+// output is rounded to bf16 once.
+static cudaError_t ring_fwd_schedule(FwdParams f, int n_groups, int per_member, size_t rows, size_t rows_per_member,
+                                     float* acc_o, float* part_o, float* part_l, float* lse, void* o,
+                                     const char* name, cudaStream_t s) {
+    const int d = f.d;
+    for (int t = 0; t < n_groups; ++t) {
+        f.ring_t = t;
+        f.ring_i0 = f.causal ? t : 0;
+        f.n_outer = (f.causal ? n_groups - t : n_groups) * per_member;
+        f.o_f32 = t == 0 ? acc_o : part_o;
+        f.lse = t == 0 ? lse : part_l;
+        cudaError_t e = traced(name, s, [&] { return launch_attn_fwd_bf16(f, s); });
+        if (e != cudaSuccess) return e;
+        if (t > 0) {
+            const size_t r0 = (size_t)f.ring_i0 * rows_per_member;
+            e = traced("ring_merge", s, [&] {
+                return launch_lse_merge((int64_t)(rows - r0), d, acc_o + r0 * d, lse + r0, part_o + r0 * d,
+                                        part_l + r0, acc_o + r0 * d, lse + r0, s);
+            });
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s); });
+}
+
+// The ring backward over n_groups members (b's tensors, workspace rows and float32 accumulators
+// set; the pre pass already run): at step t member i adds its partial gradients for the block
+// pair (i, (i - t) mod n_groups) -- dK, dV travel with the KV block, dQ stays with the queries,
+// masked only on the diagonal (t = 0).  Every block receives its first contribution at t = 0, so
+// later steps add.  The accumulators are rounded to bf16 once.
+static cudaError_t ring_bwd_schedule(BwdParams b, int n_groups, int per_member, bool causal, size_t q_elems,
+                                     size_t k_elems, void* dq, void* dk, void* dv, const char* name_dkdv,
+                                     const char* name_dq, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    for (int t = 0; e == cudaSuccess && t < n_groups; ++t) {
+        b.ring_t = t;
+        b.ring_i0 = causal ? t : 0;
+        b.n_outer = (causal ? n_groups - t : n_groups) * per_member;
+        b.causal = (causal && t == 0) ? 1 : 0;
+        b.accumulate = t > 0 ? 1 : 0;
+        e = traced(name_dkdv, s, [&] { return launch_bwd_dkdv(b, s); });
+        if (e == cudaSuccess) e = traced(name_dq, s, [&] { return launch_bwd_dq(b, s); });
+    }
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(b.dq_f32, dq, (int64_t)q_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(b.dk_f32, dk, (int64_t)k_elems, s); });
+    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(b.dv_f32, dv, (int64_t)k_elems, s); });
+    return e;
+}
+
 // Ring workspace: float32 running output [rows][d], float32 partial output
 // [rows][d] and partial LSE [rows], rows = P*B*(N/P)*Hq in sequence-sharded
 // order.  The caller's lse buffer holds the running LSE.
@@ -377,25 +431,9 @@ usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k,
     f.l_s_outer = (int64_t)Np * Hq;
     f.status = sp;
 
-    for (int t = 0; t < P; ++t) {
-        // causal: rank i attends block i - t only when that block is not in its future
-        f.ring_t = t;
-        f.ring_i0 = f.causal ? t : 0;
-        f.n_outer = (f.causal ? P - t : P) * B;
-        f.o_f32 = t == 0 ? acc_o : part_o;
-        f.lse = t == 0 ? lse : part_l;
-        cudaError_t e = traced("ring_attn_partial", s, [&] { return launch_attn_fwd_bf16(f, s); });
-        if (e != cudaSuccess) return USP_ERR_CUDA;
-        if (t > 0) {
-            const size_t r0 = (size_t)f.ring_i0 * rows_per_rank;
-            e = traced("ring_merge", s, [&] {
-                return launch_lse_merge((int64_t)(rows - r0), d, acc_o + r0 * d, lse + r0, part_o + r0 * d,
-                                        part_l + r0, acc_o + r0 * d, lse + r0, s);
-            });
-            if (e != cudaSuccess) return USP_ERR_CUDA;
-        }
-    }
-    return cuda_status(traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s); }));
+    // rank i attends block i - t only when that block is not in its future
+    return cuda_status(
+        ring_fwd_schedule(f, P, B, rows, rows_per_rank, acc_o, part_o, part_l, lse, o, "ring_attn_partial", s));
 }
 
 // Ring backward workspace: the backward rows (40 bytes per padded query row
@@ -463,23 +501,8 @@ usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k,
 
     // D and the lse rows of every rank (they use the final O and the merged LSE)
     cudaError_t e = traced("ring_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    if (e != cudaSuccess) return USP_ERR_CUDA;
-    for (int t = 0; t < P; ++t) {
-        // step t: rank i holds KV block j = (i - t) mod P (skipped when j > i under the causal mask,
-        // masked only when j == i); its dK_j, dV_j partials travel with the block, dQ_i stays on rank i.
-        // Every block receives its first contribution at t = 0, so later steps add.
-        b.ring_t = t;
-        b.ring_i0 = p->causal ? t : 0;
-        b.n_outer = (p->causal ? P - t : P) * B;
-        b.causal = (p->causal && t == 0) ? 1 : 0;
-        b.accumulate = t > 0 ? 1 : 0;
-        e = traced("ring_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
-        if (e == cudaSuccess) e = traced("ring_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
-        if (e != cudaSuccess) return USP_ERR_CUDA;
-    }
-    e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dq, dq, (int64_t)q_elems, s); });
-    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dk, dk, (int64_t)k_elems, s); });
-    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dv, dv, (int64_t)k_elems, s); });
+    if (e == cudaSuccess)
+        e = ring_bwd_schedule(b, P, B, p->causal != 0, q_elems, k_elems, dq, dk, dv, "ring_bwd_dkdv", "ring_bwd_dq", s);
     return cuda_status(e);
 }
 
@@ -1065,24 +1088,8 @@ usp_status usp_hybrid_attn_fwd(const usp_problem* p, int Pu, const void* q, cons
     f.l_s_tok = 1;
     f.l_s_outer = (int64_t)Hl * Nc;
     f.status = sp;
-    for (int t = 0; t < Pr; ++t) {
-        f.ring_t = t;
-        f.ring_i0 = f.causal ? t : 0;
-        f.n_outer = (f.causal ? Pr - t : Pr) * Pu * B;
-        f.o_f32 = t == 0 ? acc_o : part_o;
-        f.lse = t == 0 ? lse : part_l;
-        cudaError_t e = traced("hybrid_attn_partial", s, [&] { return launch_attn_fwd_bf16(f, s); });
-        if (e != cudaSuccess) return USP_ERR_CUDA;
-        if (t > 0) {
-            const size_t r0 = (size_t)f.ring_i0 * rows_per_group;
-            e = traced("ring_merge", s, [&] {
-                return launch_lse_merge((int64_t)(rows - r0), d, acc_o + r0 * d, lse + r0, part_o + r0 * d,
-                                        part_l + r0, acc_o + r0 * d, lse + r0, s);
-            });
-            if (e != cudaSuccess) return USP_ERR_CUDA;
-        }
-    }
-    return cuda_status(traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_o, o, (int64_t)(rows * d), s); }));
+    return cuda_status(ring_fwd_schedule(f, Pr, Pu * B, rows, rows_per_group, acc_o, part_o, part_l, lse, o,
+                                         "hybrid_attn_partial", s));
 }
 
 // Backward workspace: 40 bytes per padded query row of every (rank, batch, local head), then
@@ -1136,22 +1143,11 @@ usp_status usp_hybrid_attn_bwd(const usp_problem* p, int Pu, const void* q, cons
     b.scale = eff_scale(p);
     b.status = sp;
 
+    // as the ring backward, over groups: dK, dV travel with the KV chunk, dQ stays
     cudaError_t e = traced("hybrid_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    if (e != cudaSuccess) return USP_ERR_CUDA;
-    for (int t = 0; t < Pr; ++t) {
-        // as the ring backward, over groups: dK, dV travel with the KV chunk, dQ stays
-        b.ring_t = t;
-        b.ring_i0 = p->causal ? t : 0;
-        b.n_outer = (p->causal ? Pr - t : Pr) * Pu * B;
-        b.causal = (p->causal && t == 0) ? 1 : 0;
-        b.accumulate = t > 0 ? 1 : 0;
-        e = traced("hybrid_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
-        if (e == cudaSuccess) e = traced("hybrid_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
-        if (e != cudaSuccess) return USP_ERR_CUDA;
-    }
-    e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dq, dq, (int64_t)q_elems, s); });
-    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dk, dk, (int64_t)k_elems, s); });
-    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dv, dv, (int64_t)k_elems, s); });
+    if (e == cudaSuccess)
+        e = ring_bwd_schedule(b, Pr, Pu * B, p->causal != 0, q_elems, k_elems, dq, dk, dv, "hybrid_bwd_dkdv",
+                              "hybrid_bwd_dq", s);
     return cuda_status(e);
 }
 
