@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libusp.so")
-SOURCES = ["api.cu", "remap.cu", "attn_f32.cu", "attn_fwd.cu", "attn_bwd.cu", "ring.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "remap.cu", "attn_f32.cu", "attn_fwd.cu", "attn_bwd.cu", "ring.cu", "noalloc.cu", "diag.cu"]
 HEADERS = ["kernels.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

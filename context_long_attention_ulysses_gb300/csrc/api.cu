@@ -171,6 +171,13 @@ usp_status usp_device_status(usp_stream stream) {
     return USP_OK;
 }
 
+usp_status usp_diag_wait_timeout(usp_stream stream) {
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(traced("diag_wait_timeout", s, [&] { return launch_wait_timeout_probe(sp, s); }));
+}
+
 static usp_status a2a(int dir, const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
     usp_status st = check_problem(p);
     if (st != USP_OK) return st;

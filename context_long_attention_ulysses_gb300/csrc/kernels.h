@@ -116,6 +116,10 @@ cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t n, cudaStrea
 // fill float32 buffer with a constant (running LSE starts at -inf)
 cudaError_t launch_fill_f32(float* dst, float value, int64_t n, cudaStream_t stream);
 
+// ---- failure-detection probe (diag.cu): one CTA whose bounded wait gives up and records a
+// timeout in *status, then returns
+cudaError_t launch_wait_timeout_probe(int* status, cudaStream_t stream);
+
 // ---- tensor maps (api.cu)
 // 4-D bf16 tensor map over Tensor4 with box {64, 1, 128, 1} and 128-byte swizzle.
 bool make_tmap_bf16(CUtensorMap* map, const Tensor4& t, int d, int box_rows);

@@ -391,6 +391,14 @@ int usp_trace_report(usp_trace_entry* out, int max_entries);
  * cleared).  USP_ERR_CUDA if the synchronisation itself fails. */
 usp_status usp_device_status(usp_stream stream);
 
+/* Failure-detection check, without a fault: enqueues one CTA that waits on a
+ * barrier phase nothing completes.  Its bounded wait gives up after the wait
+ * limit (2 s), records a timeout in the device status word exactly as a
+ * stalled kernel would, and returns.  usp_device_status() then reports
+ * USP_ERR_TIMEOUT and clears the word; the context stays usable.  USP_OK once
+ * enqueued, USP_ERR_CUDA if the launch fails. */
+usp_status usp_diag_wait_timeout(usp_stream stream);
+
 /* Static, human-readable name of a status code. */
 const char* usp_status_string(usp_status s);
 

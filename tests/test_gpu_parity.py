@@ -444,3 +444,27 @@ def test_hybrid_reduces_to_ulysses_and_ring_bitwise(usp):
     assert from_hybrid(to_host(saved_1["lse"]), 1).tobytes() == lse_from_seq(to_host(lse_r)).tobytes()
     _status_ok(usp)
 
+
+# ---------------------------------------------------------------- failure detection
+def test_bounded_wait_times_out_and_the_context_survives(usp):
+    """A wait that nothing completes gives up after the 2 s limit: the host reads USP_ERR_TIMEOUT,
+    the word is cleared, and the next work on the same context runs and is correct."""
+    import time
+
+    import torch
+    from context_long_attention_ulysses_gb300 import _lib
+    assert usp.usp_device_status() == _lib.USP_OK
+    t0 = time.perf_counter()
+    usp.usp_diag_wait_timeout()
+    assert usp.usp_device_status() == _lib.USP_ERR_TIMEOUT   # synchronises, reads and clears the word
+    assert time.perf_counter() - t0 > 1.9                    # the wait ran to its limit
+    assert usp.usp_device_status() == _lib.USP_OK
+    p = usp.Problem(B=1, Hq=4, Hkv=4, N=512, d=128, P=2)
+    x = gen((1, 4, 512, 128), 6)
+    src = to_dev(to_seq(x, 2))
+    head = torch.empty(p.head_shape(4), dtype=torch.bfloat16, device="cuda")
+    usp.usp_a2a_seq2head(p, 4, src, head)
+    _sync()
+    assert to_host(head).tobytes() == to_head(x, 2).tobytes()
+    _status_ok(usp)
+
