@@ -55,11 +55,13 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # DRAM bytes (read + write) per launch at the 128K workload, from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; see
 # profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
-# sources they were taken on: a changed kernel reports null until re-measured.
+# sources: a changed kernel reports null until re-measured.  The figures are the
+# default instantiations' (in-place sequence-sharded addressing compiled out); an
+# edit confined to the other instantiation (if constexpr) re-keys them unchanged.
 MEASURED_TRAFFIC = {
     "attn_fwd": (2924220160 + 1160072448, "060417e63914f8b5", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (9132134144 + 526144000, "484bd2383c370539", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (4461772800 + 1050943488, "484bd2383c370539", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdv": (9132134144 + 526144000, "2fc572cbac4bdfc6", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dq": (4461772800 + 1050943488, "2fc572cbac4bdfc6", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 

@@ -336,6 +336,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tma_load_4d(sbase + C::kOffK + c * 16384, &tm_k, c * 64, hk, kv.tok, kv.outer, BAR(kKvFull));
             tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, hk, kv.tok, kv.outer, BAR(kKvFull));
         }
+        TokOuter q_next = {0, 0};  // split mode: the next query tile's coordinates, stepped through the shards
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::kStages;
             const int hq = hk * p.g + it / nq;
@@ -344,7 +345,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 !mbar_wait(BAR(kQEmpty + s), ((it / C::kStages) - 1) & 1, abort_p, 21, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kQFull + s), 2 * C::kTile + 2 * C::kXBytes);
-            const TokOuter qa = split_pos(qt * C::kBQ, q_outer, SPLIT ? p.split_np : 0, p.split_b);
+            TokOuter qa;
+            if constexpr (SPLIT) {
+                // one division per query head (the walk restarts at qt_lo), then whole tiles per shard
+                if (it % nq == 0) q_next = split_pos(qt * C::kBQ, q_outer, p.split_np, p.split_b);
+                qa = q_next;
+                q_next.tok += C::kBQ;
+                if (q_next.tok == p.split_np) {
+                    q_next.tok = 0;
+                    q_next.outer += p.split_b;
+                }
+            } else {
+                qa = {qt * C::kBQ, q_outer};
+            }
             for (int c = 0; c < C::kChunks; ++c) {
                 tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, hq, qa.tok, qa.outer,
                             BAR(kQFull + s));
