@@ -468,3 +468,91 @@ def test_bounded_wait_times_out_and_the_context_survives(usp):
     assert to_host(head).tobytes() == to_head(x, 2).tobytes()
     _status_ok(usp)
 
+
+# ---------------------------------------------------------------- writes stay inside their buffers
+def test_no_write_outside_any_buffer(usp):
+    """Every output and workspace of every path sits between 4 KiB guard regions (a fixed byte
+    pattern); after the remapped, fused, ring, zigzag, all-gather and 2-D paths ran forward and
+    backward, every guard is unchanged.  Ragged 300- and 600-token shards, two sequences, GQA."""
+    import torch
+    from tests.guarded import Guarded
+    dev = "cuda"
+    damaged = {}
+
+    def inputs(p):
+        q = to_dev(to_seq(gen((p.B, p.Hq, p.N, p.d), 0), p.P))
+        k = to_dev(to_seq(gen((p.B, p.Hkv, p.N, p.d), 1), p.P))
+        v = to_dev(to_seq(gen((p.B, p.Hkv, p.N, p.d), 2), p.P))
+        do = to_dev(to_seq(gen((p.B, p.Hq, p.N, p.d), 3), p.P))
+        return q, k, v, do
+
+    # remapped Ulysses and the fused path (shards of whole 128-row tiles)
+    p = usp.Problem(B=2, Hq=4, Hkv=2, N=512, d=128, P=2)
+    q, k, v, do = inputs(p)
+    g = Guarded()
+    qh, oh, doh, dqh = (g.empty(p.head_shape(p.Hq), torch.bfloat16, dev) for _ in range(4))
+    kh, vh, dkh, dvh = (g.empty(p.head_shape(p.Hkv), torch.bfloat16, dev) for _ in range(4))
+    lse = g.empty(p.lse_head_shape(), torch.float32, dev)
+    o, dq = g.empty_like(q), g.empty_like(q)
+    dk, dv = g.empty_like(k), g.empty_like(v)
+    ws = g.bytes(usp.usp_attn_bwd_workspace_size(p), dev)
+    usp.usp_a2a_seq2head(p, p.Hq, q, qh)
+    usp.usp_a2a_seq2head(p, p.Hkv, k, kh)
+    usp.usp_a2a_seq2head(p, p.Hkv, v, vh)
+    usp.usp_attn_fwd(p, qh, kh, vh, oh, lse)
+    usp.usp_a2a_head2seq(p, p.Hq, oh, o)
+    usp.usp_a2a_seq2head(p, p.Hq, do, doh)
+    usp.usp_attn_bwd(p, qh, kh, vh, oh, lse, doh, dqh, dkh, dvh, ws)
+    for src, dst, h in ((dqh, dq, p.Hq), (dkh, dk, p.Hkv), (dvh, dv, p.Hkv)):
+        usp.usp_a2a_head2seq(p, h, src, dst)
+    _sync()
+    damaged["remapped"] = g.damaged()
+    g = Guarded()
+    o, dq = g.empty_like(q), g.empty_like(q)
+    dk, dv = g.empty_like(k), g.empty_like(v)
+    lse = g.empty(p.lse_seq_shape(), torch.float32, dev)
+    ws = g.bytes(usp.usp_fused_attn_bwd_workspace_size(p), dev)
+    usp.usp_fused_attn_fwd(p, q, k, v, o, lse)
+    usp.usp_fused_attn_bwd(p, q, k, v, o, lse, do, dq, dk, dv, ws)
+    _sync()
+    damaged["fused"] = g.damaged()
+
+    # sequence-sharded paths on ragged shards of 300 tokens (2-D: chunks of 600)
+    p = usp.Problem(B=2, Hq=4, Hkv=2, N=1200, d=64, P=4)
+    q, k, v, do = inputs(p)
+    for name, fwd, bwd, ws_f, ws_b in (
+            ("ring", usp.usp_ring_attn_fwd, usp.usp_ring_attn_bwd, usp.usp_ring_workspace_size,
+             usp.usp_ring_bwd_workspace_size),
+            ("zigzag", usp.usp_zigzag_attn_fwd, usp.usp_zigzag_attn_bwd, usp.usp_zigzag_workspace_size,
+             usp.usp_zigzag_bwd_workspace_size),
+            ("allgather", usp.usp_allgather_attn_fwd, usp.usp_allgather_attn_bwd,
+             usp.usp_allgather_workspace_size, usp.usp_allgather_bwd_workspace_size)):
+        g = Guarded()
+        o, dq = g.empty_like(q), g.empty_like(q)
+        dk, dv = g.empty_like(k), g.empty_like(v)
+        lse = g.empty(p.lse_seq_shape(), torch.float32, dev)
+        ws, bws = g.bytes(ws_f(p), dev), g.bytes(ws_b(p), dev)
+        fwd(p, q, k, v, o, lse, ws)
+        bwd(p, q, k, v, o, lse, do, dq, dk, dv, bws)
+        _sync()
+        damaged[name] = g.damaged()
+    Pu = 2
+    g = Guarded()
+    hq, ho, hdo, hdq = (g.empty(p.hybrid_shape(p.Hq, Pu), torch.bfloat16, dev) for _ in range(4))
+    hk, hv, hdk, hdv = (g.empty(p.hybrid_shape(p.Hkv, Pu), torch.bfloat16, dev) for _ in range(4))
+    hlse = g.empty(p.lse_hybrid_shape(Pu), torch.float32, dev)
+    ws, bws = g.bytes(usp.usp_hybrid_workspace_size(p, Pu), dev), g.bytes(usp.usp_hybrid_bwd_workspace_size(p, Pu), dev)
+    o, dq = g.empty_like(q), g.empty_like(q)
+    usp.usp_hybrid_seq2head(p, Pu, p.Hq, q, hq)
+    usp.usp_hybrid_seq2head(p, Pu, p.Hkv, k, hk)
+    usp.usp_hybrid_seq2head(p, Pu, p.Hkv, v, hv)
+    usp.usp_hybrid_seq2head(p, Pu, p.Hq, do, hdo)
+    usp.usp_hybrid_attn_fwd(p, Pu, hq, hk, hv, ho, hlse, ws)
+    usp.usp_hybrid_attn_bwd(p, Pu, hq, hk, hv, ho, hlse, hdo, hdq, hdk, hdv, bws)
+    usp.usp_hybrid_head2seq(p, Pu, p.Hq, ho, o)
+    usp.usp_hybrid_head2seq(p, Pu, p.Hq, hdq, dq)
+    _sync()
+    damaged["2-D"] = g.damaged()
+    assert all(not v_ for v_ in damaged.values()), damaged
+    _status_ok(usp)
+
