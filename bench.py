@@ -53,8 +53,8 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 
 
 # DRAM bytes (read + write) per launch at the 128K workload, from one ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum; see
-# profiles/dram_traffic_128k_training_step.md), keyed to a digest of the kernel
+# capture (dram__bytes_read.sum + dram__bytes_write.sum, summarised with the
+# command that took it under profiles/), keyed to a digest of the kernel
 # sources: a changed kernel reports null until re-measured.  The figures are the
 # default instantiations' (in-place sequence-sharded addressing compiled out); an
 # edit confined to the other instantiation (if constexpr) re-keys them unchanged.

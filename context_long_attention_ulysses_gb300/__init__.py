@@ -36,7 +36,7 @@ __all__ = [
     "usp_fused_attn_fwd", "usp_fused_attn_bwd_workspace_size", "usp_fused_attn_bwd", "fused_attention_fwd",
     "fused_attention_bwd", "usp_hybrid_seq2head", "usp_hybrid_head2seq", "usp_hybrid_workspace_size",
     "usp_hybrid_bwd_workspace_size", "usp_hybrid_attn_fwd", "usp_hybrid_attn_bwd", "hybrid_attention_fwd",
-    "hybrid_attention_bwd", "usp_diag_wait_timeout",
+    "hybrid_attention_bwd", "usp_diag_wait_timeout", "usp_diag_raise_status",
 ]
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -296,6 +296,10 @@ def usp_ring_merge(rows: int, d: int, o_a, lse_a, o_b, lse_b, o, lse, stream=Non
 
 def usp_diag_wait_timeout(stream=None) -> None:
     check("usp_diag_wait_timeout", load().usp_diag_wait_timeout(_stream(stream)))
+
+
+def usp_diag_raise_status(stream=None) -> None:
+    check("usp_diag_raise_status", load().usp_diag_raise_status(_stream(stream)))
 
 
 def usp_device_status(stream=None) -> int:

@@ -34,7 +34,7 @@ SYMBOLS = (
     "usp_zigzag_workspace_size", "usp_zigzag_bwd_workspace_size", "usp_zigzag_attn_fwd", "usp_zigzag_attn_bwd",
     "usp_fused_attn_fwd", "usp_fused_attn_bwd_workspace_size", "usp_fused_attn_bwd", "usp_hybrid_seq2head",
     "usp_hybrid_head2seq", "usp_hybrid_workspace_size", "usp_hybrid_bwd_workspace_size", "usp_hybrid_attn_fwd",
-    "usp_hybrid_attn_bwd", "usp_diag_wait_timeout",
+    "usp_hybrid_attn_bwd", "usp_diag_wait_timeout", "usp_diag_raise_status",
 )
 
 
@@ -114,6 +114,7 @@ def load() -> ctypes.CDLL:
             "usp_hybrid_attn_fwd": (ci, [P, ci, vp, vp, vp, vp, vp, vp, sz, vp]),
             "usp_hybrid_attn_bwd": (ci, [P, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "usp_diag_wait_timeout": (ci, [vp]),
+            "usp_diag_raise_status": (ci, [vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

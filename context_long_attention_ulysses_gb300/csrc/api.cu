@@ -178,6 +178,13 @@ usp_status usp_diag_wait_timeout(usp_stream stream) {
     return cuda_status(traced("diag_wait_timeout", s, [&] { return launch_wait_timeout_probe(sp, s); }));
 }
 
+usp_status usp_diag_raise_status(usp_stream stream) {
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(traced("diag_raise_status", s, [&] { return launch_raise_status(sp, s); }));
+}
+
 static usp_status a2a(int dir, const usp_problem* p, int Hx, const void* src, void* dst, usp_stream stream) {
     usp_status st = check_problem(p);
     if (st != USP_OK) return st;
@@ -271,9 +278,11 @@ size_t usp_attn_bwd_workspace_size(const usp_problem* p) {
     return (((size_t)p->B * p->Hq * npad * (2 * sizeof(float) + 2 * 16)) + 255) & ~(size_t)255;
 }
 
-usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
-                        const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
-                        usp_stream stream) {
+}  // extern "C"
+
+namespace usp {
+usp_status attn_bwd_check(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, const void* dq, const void* dk, const void* dv) {
     usp_status st = check_problem(p);
     if (st != USP_OK) return st;
     if (p->d != 64 && p->d != 128) return USP_ERR_UNSUPPORTED;
@@ -282,6 +291,17 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
     const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return USP_ERR_MISALIGNED;
+    return USP_OK;
+}
+}  // namespace usp
+
+extern "C" {
+
+usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        usp_stream stream) {
+    usp_status st = attn_bwd_check(p, q, k, v, o, lse, dout, dq, dk, dv);
+    if (st != USP_OK || empty(p)) return st;
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
     if (ws_bytes < usp_attn_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
     int* sp = status_ptr();

@@ -256,7 +256,7 @@ struct KvCfg {
     static constexpr int kOffOnes = kOffX + kStages * 2 * kXBytes;
     static constexpr int kOffZero = kOffOnes + kBK * 16;
     static constexpr int kOffBar = kOffZero + 2048;
-    static constexpr int kNumBars = 1 + 2 * kStages + 5;
+    static constexpr int kNumBars = 1 + 2 * kStages + 6;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 };
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const uint32_t bar0 = sbase + C::kOffBar;
     auto BAR = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
     const int kKvFull = 0, kQFull = 1, kQEmpty = 1 + C::kStages, kSFull = 1 + 2 * C::kStages, kDPFull = kSFull + 1,
-              kPReady = kSFull + 2, kDSReady = kSFull + 3, kOReady = kSFull + 4;
+              kPReady = kSFull + 2, kDSReady = kSFull + 3, kOReady = kSFull + 4, kDrain = kSFull + 5;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int Hkv = p.Hq / p.g;
@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         mbar_init(BAR(kPReady), kKvEwWarps * 32);
         mbar_init(BAR(kDSReady), kKvEwWarps * 32);
         mbar_init(BAR(kOReady), 1);
+        mbar_init(BAR(kDrain), 1);
         fence_mbar_init();
     }
     if (warp == kKvMmaWarp) {
@@ -337,6 +338,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, hk, kv.tok, kv.outer, BAR(kKvFull));
         }
         TokOuter q_next = {0, 0};  // split mode: the next query tile's coordinates, stepped through the shards
+        int issued = 0;            // query steps whose loads were issued
         for (int it = 0; it < n_it; ++it) {
             const int s = it % C::kStages;
             const int hq = hk * p.g + it / nq;
@@ -367,7 +369,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const int64_t voff = ((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ;
             bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes, p.xl + voff, C::kXBytes, BAR(kQFull + s));
             bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes + C::kXBytes, p.xd + voff, C::kXBytes, BAR(kQFull + s));
+            issued = it + 1;
         }
+        // every issued load lands before the CTA can exit (after an abort, too)
+        mbar_drain(BAR(kKvFull), 0, 40, p.status);
+        drain_ring(BAR(kQFull), C::kStages, issued, 41, p.status);
     } else if (n_it > 0 && warp == kKvMmaWarp && lane == 0) {
         constexpr uint32_t kIdS = idesc_bf16(C::kBK, C::kBQ, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
         constexpr uint32_t kIdG = idesc_bf16(C::kBK, D, 0, 1);       // dV += P^T dO, dK += dS^T Q
@@ -434,6 +440,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 mma_commit(BAR(kOReady));
             }
         }
+        // every issued MMA completes before TMEM is freed (after an abort, too)
+        mma_commit(BAR(kDrain));
+        mbar_drain(BAR(kDrain), 0, 42, p.status);
     } else if (warp < kKvEwWarps) {
         // ---------------------------------------------------------------- element-wise warps
         const int quad = warp & 3, half = warp >> 2;
@@ -560,7 +569,7 @@ struct DqCfg {
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kKStages * kTile;
     static constexpr int kOffBar = kOffV + kVStages * kTile;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 6;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 7;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColQ = 256, kColDO = 256 + D / 2, kColDQ = 384;
 };
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     auto BAR = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
     const int kKFull = 0, kKEmpty = C::kKStages, kVFull = 2 * C::kKStages, kVEmpty = kVFull + C::kVStages,
               kSFull = kVEmpty + C::kVStages, kSFree = kSFull + 1, kDPFull = kSFull + 2, kDsReady = kSFull + 3,
-              kQdoReady = kSFull + 4, kOReady = kSFull + 5;
+              kQdoReady = kSFull + 4, kOReady = kSFull + 5, kDrain = kSFull + 6;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int n_qt = (p.N + C::kBM - 1) / C::kBM;
@@ -640,6 +649,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mbar_init(BAR(kDsReady), kDqEwWarps * 32);
         mbar_init(BAR(kQdoReady), kDqEwWarps * 32);
         mbar_init(BAR(kOReady), 1);
+        mbar_init(BAR(kDrain), 1);
         fence_mbar_init();
     }
     if (warp == kDqMmaWarp) {
@@ -655,6 +665,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (n_it > 0 && warp == kDqProducerWarp && lane == 0) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        int nk = 0, nv = 0;  // K and V tiles whose loads were issued
         for (int j = 0; j < n_it; ++j) {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
             if (j >= C::kKStages &&
@@ -665,6 +676,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_4d(sbase + C::kOffK + ks * C::kTile + c * 16384, &tm_k, c * 64, hk, kv.tok, kv.outer,
                             BAR(kKFull + ks));
+            nk = j + 1;
             if (j >= C::kVStages &&
                 !mbar_wait(BAR(kVEmpty + vs), ((j / C::kVStages) - 1) & 1, abort_p, 38, p.status))
                 break;
@@ -672,7 +684,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_4d(sbase + C::kOffV + vs * C::kTile + c * 16384, &tm_v, c * 64, hk, kv.tok, kv.outer,
                             BAR(kVFull + vs));
+            nv = j + 1;
         }
+        // every issued load lands before the CTA can exit (after an abort, too)
+        drain_ring(BAR(kKFull), C::kKStages, nk, 43, p.status);
+        drain_ring(BAR(kVFull), C::kVStages, nv, 44, p.status);
     } else if (n_it > 0 && warp == kDqMmaWarp && lane == 0) {
         constexpr uint32_t kIdS = idesc_bf16(C::kBM, C::kBN, 0, 0);  // S = Q K^T, dP = dO V^T (B K-major)
         constexpr uint32_t kIdG = idesc_bf16(C::kBM, D, 0, 1);       // dQ += dS K, K MN-major
@@ -732,6 +748,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 mma_commit(BAR(kOReady));
             }
         }
+        // every issued MMA completes before TMEM is freed (after an abort, too)
+        mma_commit(BAR(kDrain));
+        mbar_drain(BAR(kDrain), 0, 45, p.status);
     } else if (warp < kDqEwWarps) {
         const int quad = warp & 3, half = warp >> 2;
         const int r = quad * 32 + lane;  // query row within the tile = TMEM lane

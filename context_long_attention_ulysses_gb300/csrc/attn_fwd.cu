@@ -63,7 +63,7 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + kStreams * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 * kStreams;
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 * kStreams + 1;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM slot, + alignment slack
     static constexpr uint32_t kTmemCols = 512;
 };
@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kSFull = kVEmpty + C::kVStages;  // per stream
     const int kPReady = kSFull + kStreams;     // per stream
     const int kOReady = kPReady + kStreams;    // per stream
+    const int kDrain = kOReady + kStreams;     // the MMA issuer's last commit
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(kPReady + st), 4 * 32);
             mbar_init(BAR(kOReady + st), 1);
         }
+        mbar_init(BAR(kDrain), 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -213,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // coordinates of key tile j; in split mode they step through the shards (whole tiles per shard)
         TokOuter kv = {0, w.kv_outer};
+        int nk = 0, nv = 0;  // K and V tiles whose loads were issued
         for (int j = 0; j < w.n_max; ++j) {
             const int ks = j % C::kKStages, vs = j % C::kVStages;
             if (j >= C::kKStages && !mbar_wait(BAR(kKEmpty + ks), ((j / C::kKStages) - 1) & 1, abort_p, 1, p.status))
@@ -221,18 +224,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_4d(sbase + C::kOffK + ks * C::kTileBytes + c * 16384, &tm_k, c * 64, w.kv_head, kv.tok,
                             kv.outer, BAR(kKFull + ks));
+            nk = j + 1;
             if (j >= C::kVStages && !mbar_wait(BAR(kVEmpty + vs), ((j / C::kVStages) - 1) & 1, abort_p, 2, p.status))
                 break;
             mbar_arrive_expect_tx(BAR(kVFull + vs), C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_4d(sbase + C::kOffV + vs * C::kTileBytes + c * 16384, &tm_v, c * 64, w.kv_head, kv.tok,
                             kv.outer, BAR(kVFull + vs));
+            nv = j + 1;
             kv.tok += kBN;
             if (SPLIT && kv.tok == p.split_np) {
                 kv.tok = 0;
                 kv.outer += p.split_b;
             }
         }
+        // every issued load lands before the CTA can exit (after an abort, too)
+        mbar_drain(BAR(kQFull), 0, 10, p.status);
+        drain_ring(BAR(kKFull), C::kKStages, nk, 11, p.status);
+        drain_ring(BAR(kVFull), C::kVStages, nv, 12, p.status);
     } else if (w.n_max > 0 && warp == kMmaWarp && lane == 0) {
         // ---------------------------------------------------------------- MMA issuer
         constexpr uint32_t kIdS = idesc_bf16(kBM, kBN, 0, 0);  // S = Q K^T, both K-major
@@ -290,6 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(BAR(kVEmpty + vs));
             if (k_waited) mma_commit(BAR(kKEmpty + ks1));
         }
+        // every issued MMA completes before TMEM is freed (after an abort, too)
+        mma_commit(BAR(kDrain));
+        mbar_drain(BAR(kDrain), 0, 13, p.status);
     }
     } else {
         setmaxnreg_inc<kSoftmaxRegs>();

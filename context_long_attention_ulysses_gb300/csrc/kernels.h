@@ -8,6 +8,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/usp.h"
+
 namespace usp {
 
 // ---- all-to-all layout remap (remap.cu)
@@ -119,6 +121,13 @@ cudaError_t launch_fill_f32(float* dst, float value, int64_t n, cudaStream_t str
 // ---- failure-detection probe (diag.cu): one CTA whose bounded wait gives up and records a
 // timeout in *status, then returns
 cudaError_t launch_wait_timeout_probe(int* status, cudaStream_t stream);
+// sets *status as a timed-out wait would (if it is clear)
+cudaError_t launch_raise_status(int* status, cudaStream_t stream);
+
+// ---- argument checks of usp_attn_bwd that need no workspace (api.cu): the status usp_attn_bwd
+// returns for these arguments before it looks at its workspace (USP_OK for a valid or empty problem)
+usp_status attn_bwd_check(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, const void* dq, const void* dk, const void* dv);
 
 // ---- tensor maps (api.cu)
 // 4-D bf16 tensor map over Tensor4 with box {64, 1, 128, 1} and 128-byte swizzle.

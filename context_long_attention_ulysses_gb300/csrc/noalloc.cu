@@ -1,7 +1,7 @@
 // Attention backward for callers that cannot allocate device memory.
 //
-// usp_attn_bwd needs a caller-provided workspace (two float32 values per
-// query row).  Some callers cannot obtain one: code running inside a
+// usp_attn_bwd needs a caller-provided workspace (40 bytes per query row,
+// rows padded to 128-row tiles).  Some callers cannot obtain one: code running inside a
 // framework that owns every device allocation and forbids raw cudaMalloc,
 // plugins loaded into a host process that has no allocator to hand them, or
 // code that must not touch the allocator at all once set up.  This file gives
@@ -12,10 +12,14 @@
 // Every GPU that loads the library holds it until the process exits.  Host
 // code cannot use the array's name as a device address (it names a host-side
 // stand-in), so the address is looked up with cudaGetSymbolAddress once per
-// device, with that device current, on the first call made on it.
+// device, with that device current, on the first call made on it, and kept
+// for the life of the process: after cudaDeviceReset the array may sit at a
+// new address, which this cache does not see (the library's status word is
+// looked up the same way).
 #include <mutex>
 
 #include "../../include/usp.h"
+#include "kernels.h"
 
 namespace {
 
@@ -47,13 +51,15 @@ usp_status scratch_address(void** out) {
 extern "C" usp_status usp_attn_bwd_noalloc(const usp_problem* p, const void* q, const void* k, const void* v,
                                            const void* o, const float* lse, const void* dout, void* dq, void* dk,
                                            void* dv, usp_stream stream) {
-    // Size checks first: a problem the scratch cannot hold is rejected before any CUDA call.
+    // Every argument check, then the size check, before any CUDA call: a problem the backward does
+    // not support, or one the scratch cannot hold, is refused with nothing looked up or enqueued.
+    usp_status st = usp::attn_bwd_check(p, q, k, v, o, lse, dout, dq, dk, dv);
+    if (st != USP_OK) return st;
     const size_t need = usp_attn_bwd_workspace_size(p);
-    if (need == 0)  // an invalid problem (rejected) or an empty one (nothing to do): no scratch involved
-        return usp_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, nullptr, 0, stream);
+    if (need == 0) return USP_OK;  // an empty problem: nothing to do
     if (need > kScratchBytes) return USP_ERR_WORKSPACE;
     void* scratch = nullptr;
-    usp_status st = scratch_address(&scratch);
+    st = scratch_address(&scratch);
     if (st != USP_OK) return st;
     // The backward's first pass rewrites every scratch entry the later passes
     // read, so the previous call's contents never matter.

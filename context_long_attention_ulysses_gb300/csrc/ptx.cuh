@@ -78,6 +78,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Wait for a phase whose completion is already under way (TMA loads issued
+// into it, or a tcgen05.commit that tracks issued MMAs), bounded by time only:
+// unlike mbar_wait it does not give up when another role or CTA has aborted,
+// because its purpose is to let this CTA's own asynchronous work land before
+// the CTA frees its TMEM and exits.  A drain that runs out records
+// 0x44000000 | site in *status (first writer wins) and returns false.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, int site, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+            atomicCAS(status, 0, 0x44000000 | site);
+            return false;
+        }
+    }
+}
+
+// Drain a ring of `stages` full barriers (8 bytes apart from bar_first) into
+// which n loads were issued round-robin, load j into stage j % stages: wait
+// for the phase the last load of each stage completes.  No phase of a stage
+// can run past that one (nothing else arrives on it), so its parity decides.
+__device__ __forceinline__ void drain_ring(uint32_t bar_first, int stages, int n, int site, int* status) {
+    for (int s = 0; s < stages && s < n; ++s) {
+        const int issued = (n - s + stages - 1) / stages;
+        mbar_drain(bar_first + 8u * (uint32_t)s, (uint32_t)(issued - 1) & 1u, site, status);
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -156,8 +156,13 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
  * exits.  Nothing is allocated or freed by the call.
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress) with that device current; make that first
- *    call before any stream capture.
- *  - Size limit: problems needing more than USP_NOALLOC_SCRATCH_BYTES
+ *    call before any stream capture.  The address is kept for the life of the
+ *    process: after cudaDeviceReset on a device this entry point must not be
+ *    called there again (the array may have moved; the same holds for every
+ *    entry point, whose device status word is looked up the same way).
+ *  - Checks: every argument check of usp_attn_bwd (sizes, d, dtype,
+ *    pointers), then the size limit, come before any CUDA call.  Problems
+ *    needing more than USP_NOALLOC_SCRATCH_BYTES
  *    (usp_attn_bwd_workspace_size) return USP_ERR_WORKSPACE with nothing
  *    enqueued.
  *  - Sharing: every call on a device uses the same array, and the array keeps
@@ -398,6 +403,17 @@ usp_status usp_device_status(usp_stream stream);
  * USP_ERR_TIMEOUT and clears the word; the context stays usable.  USP_OK once
  * enqueued, USP_ERR_CUDA if the launch fails. */
 usp_status usp_diag_wait_timeout(usp_stream stream);
+
+/* Failure-detection check of the attention kernels' abort path, without a
+ * fault: enqueues a write of a timeout record into the device status word
+ * (if it is clear), as a wait that gave up would.  Every CTA of the kernels
+ * enqueued after it then gives up at its first wait that is not already
+ * satisfied, waits (bounded) for its own TMA loads and MMAs in flight, frees
+ * its TMEM and returns; their outputs are then undefined.
+ * usp_device_status() reports USP_ERR_TIMEOUT and clears the word, after
+ * which the context runs every path normally.  USP_OK once enqueued,
+ * USP_ERR_CUDA if the launch fails. */
+usp_status usp_diag_raise_status(usp_stream stream);
 
 /* Static, human-readable name of a status code. */
 const char* usp_status_string(usp_status s);

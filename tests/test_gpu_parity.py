@@ -469,6 +469,45 @@ def test_bounded_wait_times_out_and_the_context_survives(usp):
     _status_ok(usp)
 
 
+def test_aborted_attention_kernels_drain_and_the_context_survives(usp):
+    """The status word is set before real attention launches, so every CTA of the forward, dK/dV and
+    dQ kernels gives up at its first wait that is not yet satisfied, with its TMA loads and MMAs in
+    flight. Each CTA waits for those before it frees TMEM and exits. The launches end fast (no drain
+    ran to its 2 s limit), the host reads USP_ERR_TIMEOUT once, and the same context then gives the
+    clean run's results bit for bit."""
+    import time
+
+    import torch
+    from context_long_attention_ulysses_gb300 import _lib
+    B, Hq, Hkv, N, d, P = 1, 8, 2, 4096, 128, 2
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P)
+    q, k, v, dO = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2), gen((B, Hq, N, d), 3)
+    qh, kh, vh, doh = (to_dev(to_head(x, P)) for x in (q, k, v, dO))
+    ws = torch.empty(usp.usp_attn_bwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+
+    def run():
+        o = torch.empty_like(qh)
+        lse = torch.empty(p.lse_head_shape(), dtype=torch.float32, device="cuda")
+        grads = [torch.empty_like(qh), torch.empty_like(kh), torch.empty_like(vh)]
+        usp.usp_attn_fwd(p, qh, kh, vh, o, lse)
+        usp.usp_attn_bwd(p, qh, kh, vh, o, lse, doh, *grads, ws)
+        return [o, lse, *grads]
+
+    assert usp.usp_device_status() == _lib.USP_OK
+    clean = [to_host(t) for t in run()]
+    _sync()
+    t0 = time.perf_counter()
+    usp.usp_diag_raise_status()
+    run()
+    assert usp.usp_device_status() == _lib.USP_ERR_TIMEOUT   # synchronises, reads and clears the word
+    assert time.perf_counter() - t0 < 1.5                     # every CTA gave up fast and drained at once
+    assert usp.usp_device_status() == _lib.USP_OK
+    again = [to_host(t) for t in run()]
+    _status_ok(usp)
+    for got, want in zip(again, clean):
+        assert got.tobytes() == want.tobytes()
+
+
 # ---------------------------------------------------------------- writes stay inside their buffers
 def test_no_write_outside_any_buffer(usp):
     """Every output and workspace of every path sits between 4 KiB guard regions (a fixed byte
