@@ -91,9 +91,9 @@ def max_abs(a, b) -> float:
     return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64)))) if np.size(a) else 0.0
 
 
-def sample_rows(N: int, n: int, P: int, seed: int = 1) -> np.ndarray:
-    """n query positions without replacement, always holding the shard edges."""
-    must = {0, N - 1}
+def sample_rows(N: int, n: int, P: int, seed: int = 1, extra=()) -> np.ndarray:
+    """n positions without replacement, always holding the shard edges (and `extra`)."""
+    must = {0, N - 1, *[int(x) for x in extra]}
     Np = N // P
     for p in range(1, P):
         must.update({p * Np - 1, p * Np})

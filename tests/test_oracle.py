@@ -407,3 +407,61 @@ def test_blas_rows_closed_forms():
     vc = np.full_like(v, -1.25)
     o, _ = rows_blas.attn_rows(q, _rand((B, Hkv, N, d), 1), vc, rows, causal=False)
     np.testing.assert_allclose(o, -1.25, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_blas_full_rows_lse_dvec_and_chunked_kv_match_c_oracle(orc, causal):
+    """Every row's LSE and D_i = dO_i . O_i (chunks of 64 rows, the element-wise steps split over
+    threads) and dK/dV with query chunks of 37 rows, on a subset of KV heads, equal the C oracle."""
+    from oracle import rows_blas
+    B, Hq, Hkv, N, d = 2, 4, 2, 150, 16
+    q, k, v, dO = (_rand(s_, st, "bf16") for s_, st in (((B, Hq, N, d), 0), ((B, Hkv, N, d), 1),
+                                                         ((B, Hkv, N, d), 2), ((B, Hq, N, d), 3)))
+    dq, dk, dv, o, lse = orc.attn_bwd_full(q, k, v, dO, causal=causal)
+    dvec = np.einsum("bhnd,bhnd->bhn", orc.as_f64(dO), o)
+    lse2, dvec2 = rows_blas.attn_lse_dvec(q, k, v, dO, causal=causal, chunk=64)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dvec2, dvec, rtol=0, atol=1e-12)
+    # one KV head of one batch, rows from 70 on: the group's two query heads there, NaN elsewhere
+    lse3, dvec3 = rows_blas.attn_lse_dvec(q, k, v, dO, causal=causal, kv_heads=[(1, 0)], row_lo=70, chunk=64)
+    np.testing.assert_allclose(lse3[1, 0:2, 70:], lse[1, 0:2, 70:], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dvec3[1, 0:2, 70:], dvec[1, 0:2, 70:], rtol=0, atol=1e-12)
+    assert np.isnan(lse3[1, 0:2, :70]).all() and np.isnan(lse3[0]).all() and np.isnan(lse3[1, 2:]).all()
+    rows = np.array([0, 1, 36, 37, 74, 100, 149], dtype=np.int64)
+    dk2, dv2 = rows_blas.attn_bwd_kv_rows(q, k, v, dO, lse2, dvec2, rows, causal=causal, chunk=37)
+    np.testing.assert_allclose(dk2, dk[:, :, rows], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv2, dv[:, :, rows], rtol=0, atol=1e-11)
+    dk3, dv3 = rows_blas.attn_bwd_kv_rows(q, k, v, dO, lse2, dvec2, rows, causal=causal, chunk=37,
+                                          kv_heads=[(0, 1)])
+    np.testing.assert_allclose(dk3[0, 1], dk[0, 1][rows], rtol=0, atol=1e-11)
+    assert not dk3[0, 0].any() and not dv3[1].any()
+
+
+def test_blas_full_rows_closed_form():
+    """K = 0: every visible score is 0, so LSE_i = ln(i + 1) and O_i is the mean of V_0..V_i,
+    whence D_i = dO_i . mean_{j <= i} V_j."""
+    from oracle import rows_blas
+    B, Hq, Hkv, N, d = 1, 4, 2, 300, 8
+    q, v, dO = _rand((B, Hq, N, d), 0), _rand((B, Hkv, N, d), 2), _rand((B, Hq, N, d), 3)
+    k = np.zeros((B, Hkv, N, d), np.float32)
+    lse, dvec = rows_blas.attn_lse_dvec(q, k, v, dO, causal=True, chunk=128)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, N + 1)), lse.shape), rtol=0, atol=1e-13)
+    mean_v = np.repeat(np.cumsum(v.astype(np.float64), axis=2) / np.arange(1, N + 1)[None, None, :, None], 2, axis=1)
+    np.testing.assert_allclose(dvec, np.einsum("bhnd,bhnd->bhn", dO.astype(np.float64), mean_v), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_blas_rows_many_rows_match_c_oracle(orc, causal):
+    """Every row of 300 (three chunks, each split over several threads' row slices) equals the C
+    oracle: forward O, LSE and dQ."""
+    from oracle import rows_blas
+    B, Hq, Hkv, N, d = 1, 2, 1, 300, 16
+    q, k, v, dO = (_rand(s_, st, "bf16") for s_, st in (((B, Hq, N, d), 0), ((B, Hkv, N, d), 1),
+                                                         ((B, Hkv, N, d), 2), ((B, Hq, N, d), 3)))
+    rows = np.arange(N, dtype=np.int64)
+    o, lse = orc.attn_rows(q, k, v, rows=rows, causal=causal)
+    o2, lse2 = rows_blas.attn_rows(q, k, v, rows, causal=causal)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
+    dq = orc.attn_bwd_q_rows(q, k, v, dO, rows=rows, causal=causal)
+    np.testing.assert_allclose(rows_blas.attn_bwd_q_rows(q, k, v, dO, rows, causal=causal), dq, rtol=0, atol=1e-11)
