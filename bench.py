@@ -47,6 +47,18 @@ WORKLOADS = {
 }
 WORKLOAD, WORKLOAD_NAME = WORKLOADS["128k"]
 RING = dict(B=1, Hq=32, Hkv=32, N=524288, d=128, P=8)
+# the smaller workloads of the pages, each timed as its own leg beside the step: the tiny float32
+# exactness case (forward only), the glossary page's 4096-token example and 32000 tokens on four
+# devices (rounded to 32768), forward and backward
+CONFIG_LEGS = {
+    "c1_256_fp32": (dict(B=1, Hq=4, Hkv=4, N=256, d=64, P=2), "f32", False,
+                    "tiny exactness case: B=1, H=4, N=256, d=64, fp32, causal, P=2; remap, forward, remap"),
+    "c2_4k": (dict(B=1, Hq=4, Hkv=4, N=4096, d=64, P=2), "bf16", True,
+              "the glossary page's example shape: B=1, H=4, N=4096, d=64, bf16, causal, P=2; forward + backward"),
+    "c3_32k": (dict(B=1, Hq=32, Hkv=8, N=32768, d=128, P=4), "bf16", True,
+               "GQA long context: B=1, 32 query / 8 KV heads, d=128, N=32768, bf16, causal, P=4; "
+               "forward + backward"),
+}
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -492,6 +504,13 @@ def run_usp(args, world, rank, local):
     if args.fused and rank == 0:
         log("fused-remap and 2-D legs")
         fused = bench_fused_and_hybrid(usp, torch, dev, peaks, w)
+    configs = None
+    if args.configs and rank == 0:
+        log("smaller-workload legs")
+        configs = {}
+        for name, (cw, cdt, cbwd, desc) in CONFIG_LEGS.items():
+            configs[name] = {"workload": desc, **cw,
+                             **bench_config_leg(usp, torch, dev, peaks, cw, cdt, cbwd)}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -519,15 +538,145 @@ def run_usp(args, world, rank, local):
         line["allgather_kv"] = allgather
     if fused is not None:
         line["fused_remap"], line["hybrid_2d"] = fused
+    if configs is not None:
+        line["configs"] = configs
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         log("cpu baseline (oracle)")
         line["cpu_baseline"] = cpu_baseline(w, cpu_inputs, rows_per_head=args.cpu_rows)
+        if configs is not None:
+            log("oracle beside the smaller workloads")
+            for name, (cw, cdt, cbwd, _) in CONFIG_LEGS.items():
+                rows = None if cw["N"] <= 4096 else 64
+                line["configs"][name]["cpu_baseline"] = oracle_config(cw, cdt, cbwd, rows)
+        if ring is not None:
+            log("oracle beside the ring workload")
+            line["ring"]["cpu_baseline"] = oracle_config(RING, "bf16", True, rows_per_head=4)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def bench_config_leg(usp, torch, dev, peaks, w, dtype, backward, steps=20, warmup=3):
+    """One of the smaller workloads through the same Ulysses path as the step: remaps of Q, K, V,
+    attention forward, remap of O, and with backward the remap of dO, the backward and the remaps of
+    dQ, dK, dV.  Inputs are seeded and resident; CUDA events around `steps` steps after `warmup`."""
+    import numpy as np
+    import synth
+    p = usp.Problem(**w, causal=True, dtype=dtype)
+    Hq, Hkv = w["Hq"], w["Hkv"]
+    tdt = p.torch_dtype
+
+    def upload(shape, stream_id):
+        x = synth.normal(shape, seed=0, stream=stream_id, dtype=dtype)
+        t = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) if dtype == "bf16" else torch.from_numpy(x)
+        return t.to(dev)
+
+    qs, dos = upload(p.seq_shape(Hq), synth.STREAM_Q), upload(p.seq_shape(Hq), synth.STREAM_DO)
+    ks, vs = upload(p.seq_shape(Hkv), synth.STREAM_K), upload(p.seq_shape(Hkv), synth.STREAM_V)
+    qh, oh, doh, dqh = (torch.empty(p.head_shape(Hq), dtype=tdt, device=dev) for _ in range(4))
+    kh, vh, dkh, dvh = (torch.empty(p.head_shape(Hkv), dtype=tdt, device=dev) for _ in range(4))
+    lse = torch.empty(p.lse_head_shape(), dtype=torch.float32, device=dev)
+    os_, dqs, dks, dvs = torch.empty_like(qs), torch.empty_like(qs), torch.empty_like(ks), torch.empty_like(vs)
+    ws = torch.empty(max(1, usp.usp_attn_bwd_workspace_size(p)), dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    sh = s.cuda_stream
+
+    def step():
+        usp.usp_a2a_seq2head(p, Hq, qs, qh, sh)
+        usp.usp_a2a_seq2head(p, Hkv, ks, kh, sh)
+        usp.usp_a2a_seq2head(p, Hkv, vs, vh, sh)
+        usp.usp_attn_fwd(p, qh, kh, vh, oh, lse, sh)
+        usp.usp_a2a_head2seq(p, Hq, oh, os_, sh)
+        if backward:
+            usp.usp_a2a_seq2head(p, Hq, dos, doh, sh)
+            usp.usp_attn_bwd(p, qh, kh, vh, oh, lse, doh, dqh, dkh, dvh, ws, None, sh)
+            usp.usp_a2a_head2seq(p, Hq, dqh, dqs, sh)
+            usp.usp_a2a_head2seq(p, Hkv, dkh, dks, sh)
+            usp.usp_a2a_head2seq(p, Hkv, dvh, dvs, sh)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    usp.usp_trace_reset()
+    usp.usp_trace_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    usp.usp_trace_enable(False)
+    trace = usp.usp_trace_report()
+    ms = e0.elapsed_time(e1) / steps
+    ok = usp.usp_device_status(sh) == 0
+    f = (3.5 if backward else 1.0) * fwd_flops(w)
+    esz = 2 if dtype == "bf16" else 4
+    q_bytes = w["B"] * Hq * w["N"] * w["d"] * esz
+    kv_bytes = w["B"] * Hkv * w["N"] * w["d"] * esz
+    # read + write bytes of every tensor moved: Q, K, V and O, plus dO, dQ, dK and dV with backward
+    remap_bytes = 2 * (2 * q_bytes + 2 * kv_bytes) if not backward else 2 * (4 * q_bytes + 4 * kv_bytes)
+    remap_ms = sum(v_[1] for n_, v_ in trace.items() if n_.startswith("a2a_")) / steps
+    remap_gbs = remap_bytes / (remap_ms * 1e-3) / 1e9 if remap_ms > 0 else None
+    tflops = f / (ms * 1e-3) / 1e12
+    leg = {"ms_per_step": ms, "TFLOPs": tflops, "flops_per_step": f, "tokens_per_s": w["B"] * w["N"] / (ms * 1e-3),
+           "remap": {"GBps": remap_gbs, "bytes_per_step": remap_bytes, "ms_per_step": remap_ms,
+                     "frac_of_measured_hbm": remap_gbs / peaks["hbm"] if remap_gbs else None,
+                     "frac_of_8TBps": remap_gbs / 8000.0 if remap_gbs else None},
+           "kernels_ms_per_step": {k_: v_[1] / steps for k_, v_ in trace.items()},
+           "launches_per_step": sum(v_[0] for v_ in trace.values()) // steps,
+           "steps": steps, "warmup": warmup, "status_ok": ok}
+    if dtype == "bf16":
+        leg["frac_sustained"] = tflops / peaks["bf16_sus"]
+        leg["frac_burst"] = tflops / peaks["bf16"]
+        leg["bound"] = "tensor" if w["N"] >= 16384 else "launch (a few microseconds of work per kernel)"
+    else:
+        leg["bound"] = "launch (float32 CUDA-core forward of 33.7 MFLOP in three launches)"
+    del qs, dos, ks, vs, qh, oh, doh, dqh, kh, vh, dkh, dvh, lse, os_, dqs, dks, dvs, ws
+    torch.cuda.empty_cache()
+    return leg
+
+
+def oracle_config(w, dtype, backward, rows_per_head=None):
+    """The float64 oracle on one smaller workload, timed on the host cores: every row (forward, and
+    with backward dQ, dK, dV) when rows_per_head is None, else forward and dQ of seeded query rows,
+    extrapolated to every row by the visible pairs."""
+    import numpy as np
+    import oracle
+    import synth
+    B, Hq, Hkv, N, d = w["B"], w["Hq"], w["Hkv"], w["N"], w["d"]
+    q = synth.normal((B, Hq, N, d), seed=0, stream=synth.STREAM_Q, dtype=dtype)
+    k = synth.normal((B, Hkv, N, d), seed=0, stream=synth.STREAM_K, dtype=dtype)
+    v = synth.normal((B, Hkv, N, d), seed=0, stream=synth.STREAM_V, dtype=dtype)
+    do = synth.normal((B, Hq, N, d), seed=0, stream=synth.STREAM_DO, dtype=dtype)
+    all_pairs = float(causal_pairs(N)) * B * Hq
+    if rows_per_head is None:
+        t0 = time.perf_counter()
+        if backward:
+            oracle.attn_bwd_full(q, k, v, do, causal=True)
+        else:
+            oracle.attn_rows(q, k, v, causal=True)
+        dt = time.perf_counter() - t0
+        # executed f64 FLOPs: forward 4*d per visible pair; the backward recomputes P and O (4*d), then
+        # dP, dQ, dK, dV (8*d)
+        flops = (16.0 if backward else 4.0) * d * all_pairs
+        what = "every row: forward" + (" and dQ, dK, dV" if backward else " O and LSE")
+        return {"value": flops / dt / 1e9, "unit": "GFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                "seconds": dt, "sample": f"float64 oracle, {what} of the whole workload"}
+    rng = np.random.default_rng(11)
+    rows = np.sort(rng.choice(N, size=rows_per_head, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, rows=rows, causal=True)
+    oracle.attn_bwd_q_rows(q, k, v, do, rows=rows, causal=True)
+    dt = time.perf_counter() - t0
+    pairs = float(np.sum(rows + 1)) * B * Hq
+    return {"value": 12.0 * d * pairs / dt / 1e9, "unit": "GFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+            "seconds": dt, "extrapolated_full_fwd_dq_s": dt * all_pairs / pairs,
+            "sample": f"float64 oracle, forward O/LSE and dQ of {rows_per_head} seeded query rows per head x "
+                      f"{B * Hq} heads (12*d f64 FLOPs per visible pair); extrapolated_full_fwd_dq_s scales it "
+                      "to every row by the visible pairs"}
 
 
 def bench_allgather(usp, torch, dev, peaks, w):
@@ -810,6 +959,8 @@ def main():
                     help="skip the all-gather-KV leg (one forward and one backward on the step's workload)")
     ap.add_argument("--no-fused", dest="fused", action="store_false",
                     help="skip the fused-remap and 2-D (Ulysses x ring) legs on the step's workload")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the legs of the smaller workloads (256 fp32, 4K and 32K tokens)")
     args = ap.parse_args()
     global WORKLOAD, WORKLOAD_NAME
     WORKLOAD, WORKLOAD_NAME = WORKLOADS[args.workload]
