@@ -289,6 +289,12 @@ def kernel_work(name: str, w, launches: int):
         return "tensor", 2.0 * f               # S^T, dP^T, dV, dK: 8*d per visible pair
     if name == "attn_bwd_dq":
         return "tensor", 1.5 * f               # S, dP, dQ: 6*d per visible pair
+    if name == "attn_bwd_dkdvq":
+        return "tensor", 2.5 * f               # S^T, dP^T, dV, dK, dQ: 10*d per visible pair
+    if name == "attn_bwd_dq_zero":
+        return "hbm", B * Hq * npad * d * 4    # the float32 dQ accumulator written
+    if name == "attn_bwd_dq_store":
+        return "hbm", B * Hq * npad * d * 4 + q_bytes  # the accumulator read, dQ (bf16) written
     if name == "attn_bwd_pre":
         # reads O, dO and lse; writes D, lse*log2(e) (float32) and two 16-byte split rows per padded row
         return "hbm", 2 * q_bytes + B * Hq * N * 4 + B * Hq * npad * (2 * 4 + 2 * 16)

@@ -37,6 +37,7 @@ __all__ = [
     "fused_attention_bwd", "usp_hybrid_seq2head", "usp_hybrid_head2seq", "usp_hybrid_workspace_size",
     "usp_hybrid_bwd_workspace_size", "usp_hybrid_attn_fwd", "usp_hybrid_attn_bwd", "hybrid_attention_fwd",
     "hybrid_attention_bwd", "usp_diag_wait_timeout", "usp_diag_raise_status",
+    "usp_attn_bwd_deterministic_workspace_size", "usp_attn_bwd_deterministic",
 ]
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -150,8 +151,20 @@ def usp_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream
                                               _stream(stream)))
 
 
+def usp_attn_bwd_deterministic_workspace_size(p) -> int:
+    return int(load().usp_attn_bwd_deterministic_workspace_size(_prob(p)))
+
+
+def usp_attn_bwd_deterministic(p, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+    check("usp_attn_bwd_deterministic",
+          load().usp_attn_bwd_deterministic(_prob(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
 def usp_attn_bwd_noalloc(p, q, k, v, o, lse, dout, dq, dk, dv, stream=None) -> None:
-    """usp_attn_bwd with the library's built-in scratch instead of a workspace.
+    """usp_attn_bwd_deterministic with the library's built-in scratch instead of a workspace.
 
     For callers that cannot allocate device memory.  Problems needing more
     than NOALLOC_SCRATCH_BYTES of workspace raise UspError (USP_ERR_WORKSPACE);
@@ -360,19 +373,22 @@ def ulysses_attention_fwd(p: Problem, q_seq, k_seq, v_seq, stream=None):
     return o_seq, {"q": qh, "k": kh, "v": vh, "o": oh, "lse": lse}
 
 
-def ulysses_attention_bwd(p: Problem, saved, do_seq, stream=None):
+def ulysses_attention_bwd(p: Problem, saved, do_seq, stream=None, deterministic=False):
     """Backward of :func:`ulysses_attention_fwd` for upstream gradient dO (sequence-sharded).
 
-    Returns (dq_seq, dk_seq, dv_seq).
+    Returns (dq_seq, dk_seq, dv_seq).  deterministic=True runs the bit-reproducible three-pass
+    backward (usp_attn_bwd_deterministic) instead of the one-pass one.
     """
     dev, dt = do_seq.device, p.torch_dtype
     doh = _empty(p.head_shape(p.Hq), dt, dev)
     dqh = _empty(p.head_shape(p.Hq), dt, dev)
     dkh = _empty(p.head_shape(p.Hkv), dt, dev)
     dvh = _empty(p.head_shape(p.Hkv), dt, dev)
-    ws = torch.empty(max(usp_attn_bwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    size = usp_attn_bwd_deterministic_workspace_size(p) if deterministic else usp_attn_bwd_workspace_size(p)
+    ws = torch.empty(max(size, 256), dtype=torch.uint8, device=dev)
     usp_a2a_seq2head(p, p.Hq, do_seq, doh, stream)
-    usp_attn_bwd(p, saved["q"], saved["k"], saved["v"], saved["o"], saved["lse"], doh, dqh, dkh, dvh, ws, None, stream)
+    bwd = usp_attn_bwd_deterministic if deterministic else usp_attn_bwd
+    bwd(p, saved["q"], saved["k"], saved["v"], saved["o"], saved["lse"], doh, dqh, dkh, dvh, ws, None, stream)
     dq = _empty(p.seq_shape(p.Hq), dt, dev)
     dk = _empty(p.seq_shape(p.Hkv), dt, dev)
     dv = _empty(p.seq_shape(p.Hkv), dt, dev)

@@ -35,6 +35,7 @@ SYMBOLS = (
     "usp_fused_attn_fwd", "usp_fused_attn_bwd_workspace_size", "usp_fused_attn_bwd", "usp_hybrid_seq2head",
     "usp_hybrid_head2seq", "usp_hybrid_workspace_size", "usp_hybrid_bwd_workspace_size", "usp_hybrid_attn_fwd",
     "usp_hybrid_attn_bwd", "usp_diag_wait_timeout", "usp_diag_raise_status",
+    "usp_attn_bwd_deterministic_workspace_size", "usp_attn_bwd_deterministic",
 )
 
 
@@ -115,6 +116,8 @@ def load() -> ctypes.CDLL:
             "usp_hybrid_attn_bwd": (ci, [P, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "usp_diag_wait_timeout": (ci, [vp]),
             "usp_diag_raise_status": (ci, [vp]),
+            "usp_attn_bwd_deterministic_workspace_size": (sz, [P]),
+            "usp_attn_bwd_deterministic": (ci, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

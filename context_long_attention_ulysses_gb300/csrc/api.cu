@@ -270,12 +270,23 @@ usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, cons
     return cuda_status(traced("attn_fwd", s, [&] { return launch_attn_fwd_bf16(f, s); }));
 }
 
-size_t usp_attn_bwd_workspace_size(const usp_problem* p) {
-    if (check_problem(p) != USP_OK) return 0;
-    // per query row, rows padded to whole 128-row tiles: D_i and lse_i*log2(e) (float32), then
-    // -lse_i/scale and -D_i each as a 16-byte row of three bf16 numbers
+// Backward workspace rows: per query row, rows padded to whole 128-row tiles, D_i and lse_i*log2(e)
+// (float32), then -lse_i/scale and -D_i each as a 16-byte row of three bf16 numbers.
+static size_t bwd_rows_bytes(const usp_problem* p) {
     const size_t npad = ((size_t)p->N + 127) / 128 * 128;
     return (((size_t)p->B * p->Hq * npad * (2 * sizeof(float) + 2 * 16)) + 255) & ~(size_t)255;
+}
+
+// The one-pass backward adds the float32 dQ accumulator: d values per padded query row.
+size_t usp_attn_bwd_workspace_size(const usp_problem* p) {
+    if (check_problem(p) != USP_OK) return 0;
+    const size_t npad = ((size_t)p->N + 127) / 128 * 128;
+    return bwd_rows_bytes(p) + (size_t)p->B * p->Hq * npad * (size_t)p->d * sizeof(float);
+}
+
+size_t usp_attn_bwd_deterministic_workspace_size(const usp_problem* p) {
+    if (check_problem(p) != USP_OK) return 0;
+    return bwd_rows_bytes(p);
 }
 
 }  // extern "C"
@@ -297,16 +308,10 @@ usp_status attn_bwd_check(const usp_problem* p, const void* q, const void* k, co
 
 extern "C" {
 
-usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
-                        const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
-                        usp_stream stream) {
-    usp_status st = attn_bwd_check(p, q, k, v, o, lse, dout, dq, dk, dv);
-    if (st != USP_OK || empty(p)) return st;
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
-    if (ws_bytes < usp_attn_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
-    int* sp = status_ptr();
-    if (!sp) return USP_ERR_CUDA;
-    // head-sharded buffers as Z = B*Hq query heads (Z/g KV heads) of N tokens, one outer index
+// Head-sharded buffers as Z = B*Hq query heads (Z/g KV heads) of N tokens, one outer index.
+static BwdParams head_sharded_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                                  int* sp) {
     const int Z = p->B * p->Hq, Zk = p->B * p->Hkv, d = p->d, N = p->N;
     const int64_t nd = (int64_t)N * d;
     BwdParams b{};
@@ -328,6 +333,44 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
     b.ring_i0 = 0; b.ring_t = 0; b.ring_p = 1; b.bsz = 1; b.n_outer = 1;
     b.scale = eff_scale(p);
     b.status = sp;
+    return b;
+}
+
+// The one-pass backward: dQ accumulator zeroed, workspace rows, dK/dV/dQ-partials, dQ rounded.
+static cudaError_t one_pass_bwd(BwdParams b, const usp_problem* p, void* ws, const char* const names[4],
+                                cudaStream_t s) {
+    b.dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + bwd_rows_bytes(p));
+    cudaError_t e = traced(names[0], s, [&] { return launch_bwd_dq_zero(b, s); });
+    if (e == cudaSuccess) e = traced(names[1], s, [&] { return launch_bwd_pre(b, s); });
+    if (e == cudaSuccess) e = traced(names[2], s, [&] { return launch_bwd_dkdvq(b, s); });
+    if (e == cudaSuccess) e = traced(names[3], s, [&] { return launch_bwd_dq_store(b, s); });
+    return e;
+}
+
+usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        usp_stream stream) {
+    usp_status st = attn_bwd_check(p, q, k, v, o, lse, dout, dq, dk, dv);
+    if (st != USP_OK || empty(p)) return st;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    if (ws_bytes < usp_attn_bwd_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    const BwdParams b = head_sharded_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, sp);
+    static const char* const names[4] = {"attn_bwd_dq_zero", "attn_bwd_pre", "attn_bwd_dkdvq", "attn_bwd_dq_store"};
+    return cuda_status(one_pass_bwd(b, p, ws, names, static_cast<cudaStream_t>(stream)));
+}
+
+usp_status usp_attn_bwd_deterministic(const usp_problem* p, const void* q, const void* k, const void* v,
+                                      const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                      void* ws, size_t ws_bytes, usp_stream stream) {
+    usp_status st = attn_bwd_check(p, q, k, v, o, lse, dout, dq, dk, dv);
+    if (st != USP_OK || empty(p)) return st;
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return USP_ERR_MISALIGNED;
+    if (ws_bytes < usp_attn_bwd_deterministic_workspace_size(p)) return USP_ERR_WORKSPACE;
+    int* sp = status_ptr();
+    if (!sp) return USP_ERR_CUDA;
+    const BwdParams b = head_sharded_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, sp);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = traced("attn_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
     if (e == cudaSuccess) e = traced("attn_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
@@ -995,11 +1038,9 @@ usp_status usp_fused_attn_bwd(const usp_problem* p, const void* q, const void* k
     b.split_b = B;
     b.scale = eff_scale(p);
     b.status = sp;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = traced("fused_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    if (e == cudaSuccess) e = traced("fused_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
-    if (e == cudaSuccess) e = traced("fused_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
-    return cuda_status(e);
+    static const char* const names[4] = {"fused_bwd_dq_zero", "fused_bwd_pre", "fused_bwd_dkdvq",
+                                          "fused_bwd_dq_store"};
+    return cuda_status(one_pass_bwd(b, p, ws, names, static_cast<cudaStream_t>(stream)));
 }
 
 // ---- 2-D (hybrid) sequence parallelism: Ulysses inside groups, ring across them

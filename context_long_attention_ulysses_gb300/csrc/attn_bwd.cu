@@ -29,6 +29,7 @@
 // overwrite TMEM only after their own loads of it have completed, or after a
 // barrier says the MMA that reads it is done.  Each kernel's comment gives its
 // column plan.
+#include <algorithm>
 #include <cmath>
 
 #include "kernels.h"
@@ -147,6 +148,7 @@ struct DevBwd {
     int64_t q_s_head, q_s_tok, q_s_outer;  // dq strides (elements)
     int64_t k_s_head, k_s_tok, k_s_outer;  // dk, dv strides
     int* status;
+    float* dq_acc;  // one-pass backward: float32 dQ accumulator (BwdParams::dq_acc layout)
 };
 
 // Outer index o of a launch -> query outer (rank i, batch b), KV outer (rank
@@ -852,6 +854,467 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
 }
 
+
+// ------------------------------------------------------------------ one pass: dK, dV and dQ
+// The dK/dV walk of pass 2 with the dQ product added, so that S and dP are
+// computed (and their exponentials taken) once per visible block pair: five
+// 128 x 128 products per step (S^T, dP^T, dV, dK, dQ) instead of the four of
+// pass 2 plus the three of pass 3.
+//   dQ_i (+)= dS_i K   over this CTA's 128 keys is a partial of dQ_i; it is
+//   added in float32 into the workspace accumulator with red.global.add.v4
+//   (the CTAs of the other key tiles add theirs; the order of the additions
+//   varies from run to run, so dQ is not bit-reproducible, unlike dK and dV,
+//   which stay in TMEM for the whole walk).
+// dS^T (bf16) goes to shared memory, where it is the A operand of both
+// dK += dS^T Q (K-major) and dQ = dS K (the same bytes read M-major).  At
+// d = 128 it is written over the dO tile of its own step once dV, the last
+// product reading that tile, is done (no room for a buffer of its own).
+// TMEM: S^T (P^T in place, bf16), dP^T, dV, dK; dQ(i) lands in the dP^T
+// columns after the element-wise warps have loaded dP^T(i), and dP^T(i+1) is
+// issued after they have drained dQ(i).  Per step the tensor core runs
+//     dK(i)  dQ(i)  | dV(i+1)  dP^T(i+1)  S^T(i+2) | dK(i+1) ...
+// and the element-wise warps compute P(i+1) while dK(i) and dQ(i) run,
+// drain dQ(i) while dV(i+1) runs, and dS(i+1) while S^T(i+2) runs.  Q tiles
+// are released after dK, dO tiles (with dS^T) after dQ, so the next Q tile
+// loads while dQ and dV run.  The lse / D rows enter S^T and dP^T as the
+// ninth k-step of pass 2.
+constexpr int kKqEwWarps = 8;
+constexpr int kKqProducerWarp = 8;
+constexpr int kKqMmaWarp = 9;
+constexpr int kKqThreads = 10 * 32;
+
+template <int D>
+struct KqCfg {
+    static constexpr int kBK = 128;  // keys per CTA (TMEM lanes of S^T, dP^T, dV, dK)
+    static constexpr int kBQ = 128;  // query rows per step (TMEM lanes of dQ)
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTile = kChunks * 128 * 128;   // one 128-row bf16 tile (K, V, Q or dO)
+    static constexpr int kDsBytes = 128 * 128 * 2;     // dS^T: 128 keys x 128 queries, bf16
+    static constexpr bool kDsInDo = kTile == kDsBytes;  // d = 128: dS^T over its step's dO tile
+    static constexpr int kStages = 2;
+    static constexpr int kXBytes = kBQ * 16;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kTile;
+    static constexpr int kOffQ = 2 * kTile;
+    static constexpr int kOffDO = kOffQ + kStages * kTile;
+    static constexpr int kOffDS = kOffDO + kStages * kTile;             // d = 64: dS^T's own buffer
+    static constexpr int kOffX = kOffDS + (kDsInDo ? 0 : kDsBytes);     // per stage: lse rows, D rows
+    static constexpr int kOffOnes = kOffX + kStages * 2 * kXBytes;
+    static constexpr int kOffZero = kOffOnes + kBK * 16;
+    static constexpr int kOffBar = kOffZero + 2048;
+    static constexpr int kNumBars = 1 + 4 * kStages + 9;
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+};
+static_assert(KqCfg<128>::kSmemBytes <= 227 * 1024 && KqCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ void red_add_v4(float* a, float x, float y, float z, float w) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(a), "f"(x), "f"(y), "f"(z), "f"(w)
+                 : "memory");
+}
+
+template <int D, bool SPLIT>
+__global__ void __launch_bounds__(kKqThreads, 1)
+    dkdvq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const DevBwd p) {
+    using C = KqCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + C::kNumBars * 8);
+    __shared__ int abort_flag;
+    const uint32_t bar0 = sbase + C::kOffBar;
+    auto BAR = [&](int idx) { return bar0 + 8u * (uint32_t)idx; };
+    const int kKvFull = 0, kQFull = 1, kQEmpty = 1 + S, kOFull = 1 + 2 * S, kOEmpty = 1 + 3 * S,
+              kSFull = 1 + 4 * S, kDPFull = kSFull + 1, kPReady = kSFull + 2, kDVDone = kSFull + 3,
+              kDSReady = kSFull + 4, kDQFull = kSFull + 5, kDQFree = kSFull + 6, kOReady = kSFull + 7,
+              kDrain = kSFull + 8;
+    // shared-memory offset of step it's dS^T
+    auto ds_off = [](int it) { return C::kDsInDo ? C::kOffDO + (it % S) * C::kTile : C::kOffDS; };
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int Hkv = p.Hq / p.g;
+    // group-major: all key tiles of one (outer index, KV head), low key tiles first (as pass 2)
+    const int n_kt = (p.Nkv + C::kBK - 1) / C::kBK;
+    const int grp = blockIdx.x / n_kt;
+    const int kt = blockIdx.x % n_kt;
+    const int hk = grp % Hkv;
+    int q_outer, kv_outer, shift;
+    bwd_outer(p, grp / Hkv, q_outer, kv_outer, shift);
+    const int n_qt = (p.N + C::kBQ - 1) / C::kBQ;
+    const int first_q = kt * C::kBK - shift;
+    const int qt_lo = (p.causal && first_q > 0) ? first_q / C::kBQ : 0;
+    const int nq = max(0, n_qt - qt_lo);
+    const int n_it = p.g * nq;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(BAR(kKvFull), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(BAR(kQFull + s), 1);
+            mbar_init(BAR(kQEmpty + s), 1);
+            mbar_init(BAR(kOFull + s), 1);
+            mbar_init(BAR(kOEmpty + s), 1);
+        }
+        mbar_init(BAR(kSFull), 1);
+        mbar_init(BAR(kDPFull), 1);
+        mbar_init(BAR(kPReady), kKqEwWarps * 32);
+        mbar_init(BAR(kDVDone), 1);
+        mbar_init(BAR(kDSReady), kKqEwWarps * 32);
+        mbar_init(BAR(kDQFull), 1);
+        mbar_init(BAR(kDQFree), kKqEwWarps * 32);
+        mbar_init(BAR(kOReady), 1);
+        mbar_init(BAR(kDrain), 1);
+        fence_mbar_init();
+    }
+    if (warp == kKqMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x < C::kBK) {
+        // row t of the ones operand (bf16 1.0 in its first three columns) and 16 bytes of zeros
+        *reinterpret_cast<uint4*>(smem + C::kOffOnes + threadIdx.x * 16) = make_uint4(0x3F803F80u, 0x3F80u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + C::kOffZero + threadIdx.x * 16) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    volatile int* abort_p = &abort_flag;
+
+    if (n_it > 0 && warp == kKqProducerWarp && lane == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(BAR(kKvFull), 2 * C::kTile);
+        const TokOuter kv = split_pos(kt * C::kBK, kv_outer, SPLIT ? p.split_np : 0, p.split_b);
+        for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_4d(sbase + C::kOffK + c * 16384, &tm_k, c * 64, hk, kv.tok, kv.outer, BAR(kKvFull));
+            tma_load_4d(sbase + C::kOffV + c * 16384, &tm_v, c * 64, hk, kv.tok, kv.outer, BAR(kKvFull));
+        }
+        TokOuter q_next = {0, 0};  // split mode: the next query tile's coordinates, stepped through the shards
+        int nq_issued = 0, no_issued = 0;  // Q and dO tiles whose loads were issued
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % S;
+            const int hq = hk * p.g + it / nq;
+            const int qt = qt_lo + it % nq;
+            TokOuter qa;
+            if constexpr (SPLIT) {
+                if (it % nq == 0) q_next = split_pos(qt * C::kBQ, q_outer, p.split_np, p.split_b);
+                qa = q_next;
+                q_next.tok += C::kBQ;
+                if (q_next.tok == p.split_np) {
+                    q_next.tok = 0;
+                    q_next.outer += p.split_b;
+                }
+            } else {
+                qa = {qt * C::kBQ, q_outer};
+            }
+            const int64_t voff = ((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ;
+            // Q (with the lse rows): its stage is free once dK of step it - S is done
+            if (it >= S && !mbar_wait(BAR(kQEmpty + s), ((it / S) - 1) & 1, abort_p, 50, p.status)) break;
+            mbar_arrive_expect_tx(BAR(kQFull + s), C::kTile + C::kXBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(sbase + C::kOffQ + s * C::kTile + c * 16384, &tm_q, c * 64, hq, qa.tok, qa.outer,
+                            BAR(kQFull + s));
+            bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes, p.xl + voff, C::kXBytes, BAR(kQFull + s));
+            nq_issued = it + 1;
+            // dO (with the D rows): its stage (and the dS^T over it) is free once dQ of step it - S is done
+            if (it >= S && !mbar_wait(BAR(kOEmpty + s), ((it / S) - 1) & 1, abort_p, 51, p.status)) break;
+            mbar_arrive_expect_tx(BAR(kOFull + s), C::kTile + C::kXBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(sbase + C::kOffDO + s * C::kTile + c * 16384, &tm_do, c * 64, hq, qa.tok, qa.outer,
+                            BAR(kOFull + s));
+            bulk_load(sbase + C::kOffX + s * 2 * C::kXBytes + C::kXBytes, p.xd + voff, C::kXBytes, BAR(kOFull + s));
+            no_issued = it + 1;
+        }
+        // every issued load lands before the CTA can exit (after an abort, too)
+        mbar_drain(BAR(kKvFull), 0, 53, p.status);
+        drain_ring(BAR(kQFull), S, nq_issued, 54, p.status);
+        drain_ring(BAR(kOFull), S, no_issued, 55, p.status);
+    } else if (n_it > 0 && warp == kKqMmaWarp && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        constexpr uint32_t kIdS = idesc_bf16(C::kBK, C::kBQ, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
+        constexpr uint32_t kIdG = idesc_bf16(C::kBK, D, 0, 1);       // dV += P^T dO, dK += dS^T Q
+        constexpr uint32_t kIdQ = idesc_bf16(C::kBQ, D, 1, 1);       // dQ = dS K: A and B M/N-major
+        const uint64_t dk0 = sdesc_sw128(sbase + C::kOffK, 16, 1024), dv0 = sdesc_sw128(sbase + C::kOffV, 16, 1024);
+        const uint64_t k_mn = sdesc_sw128(sbase + C::kOffK, 16384, 1024);  // K as the N-major B of dQ
+        auto plain = [&](int off) { return sdesc_plain(sbase + off, (uint32_t)(C::kOffZero - off), 128); };
+        const uint64_t dones = plain(C::kOffOnes);
+        // S'^T (A = K, x = 0: lse rows, B = Q) or dP'^T (A = V, x = 1: D rows, B = dO) of step it
+        auto issue_t = [&](int it, uint64_t a0, int off_b, uint32_t col, int x) {
+            const int s = it % S;
+            const uint64_t b0 = sdesc_sw128(sbase + off_b + s * C::kTile, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                mma_ss(tmem + col, a0 + off, b0 + off, kIdS, kk > 0);
+            }
+            mma_ss(tmem + col, dones, plain(C::kOffX + (2 * s + x) * C::kXBytes), kIdS, 1u);
+        };
+        // dV += P^T dO: A = P^T from TMEM (the bf16 half of each 64-column block of S^T), B = dO N-major
+        auto issue_dv = [&](int it) {
+            const uint64_t b0 = sdesc_sw128(sbase + C::kOffDO + (it % S) * C::kTile, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < C::kBQ / 16; ++kk) {
+                const uint32_t a = tmem + C::kColS + (kk / 4) * 64 + (kk % 4) * 8;
+                mma_ts(tmem + C::kColDV, a, b0 + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
+            }
+        };
+        // dK += dS^T Q: A = dS^T K-major (queries 16 kk .. + 15), B = Q N-major
+        auto issue_dk = [&](int it) {
+            const uint64_t a0 = sdesc_sw128(sbase + ds_off(it), 16, 1024);
+            const uint64_t b0 = sdesc_sw128(sbase + C::kOffQ + (it % S) * C::kTile, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < C::kBQ / 16; ++kk)
+                mma_ss(tmem + C::kColDK, a0 + (((kk / 4) * 16384 + (kk % 4) * 32) >> 4), b0 + (kk * 2048 >> 4), kIdG,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+        };
+        // dQ = dS K into the dP^T columns: A = the dS^T bytes read M-major (keys 16 kk .. + 15), B = K N-major
+        auto issue_dq = [&](int it) {
+            const uint64_t a0 = sdesc_sw128(sbase + ds_off(it), 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < C::kBK / 16; ++kk)
+                mma_ss(tmem + C::kColDP, a0 + (kk * 2048 >> 4), k_mn + (kk * 2048 >> 4), kIdQ, kk > 0 ? 1u : 0u);
+        };
+        bool ok = mbar_wait(BAR(kKvFull), 0, abort_p, 56, p.status);
+        ok = ok && mbar_wait(BAR(kQFull), 0, abort_p, 57, p.status);
+        ok = ok && mbar_wait(BAR(kOFull), 0, abort_p, 58, p.status);
+        if (ok) {
+            tc_fence_after();
+            issue_t(0, dk0, C::kOffQ, C::kColS, 0);
+            mma_commit(BAR(kSFull));
+            issue_t(0, dv0, C::kOffDO, C::kColDP, 1);
+            mma_commit(BAR(kDPFull));
+        }
+        ok = ok && mbar_wait(BAR(kPReady), 0, abort_p, 59, p.status);
+        if (ok) {
+            tc_fence_after();
+            issue_dv(0);
+            mma_commit(BAR(kDVDone));
+        }
+        if (ok && n_it > 1) {
+            ok = mbar_wait(BAR(kQFull + 1 % S), (1 / S) & 1, abort_p, 57, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_t(1, dk0, C::kOffQ, C::kColS, 0);  // after dV(0), which read P^T from these columns
+                mma_commit(BAR(kSFull));
+            }
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int s = it % S;
+            if (!mbar_wait(BAR(kDSReady), it & 1, abort_p, 60, p.status)) break;
+            tc_fence_after();
+            issue_dk(it);
+            mma_commit(BAR(kQEmpty + s));
+            issue_dq(it);  // into the dP^T columns: the element-wise warps loaded dP^T(it) before dS(it)
+            mma_commit(BAR(kDQFull));
+            mma_commit(BAR(kOEmpty + s));
+            if (it + 1 < n_it) {
+                const int s1 = (it + 1) % S;
+                if (!mbar_wait(BAR(kPReady), (it + 1) & 1, abort_p, 59, p.status)) break;
+                if (!mbar_wait(BAR(kOFull + s1), ((it + 1) / S) & 1, abort_p, 58, p.status)) break;
+                tc_fence_after();
+                issue_dv(it + 1);
+                mma_commit(BAR(kDVDone));
+                // dP^T(it+1) overwrites dQ(it): after the element-wise warps have drained it
+                if (!mbar_wait(BAR(kDQFree), it & 1, abort_p, 61, p.status)) break;
+                tc_fence_after();
+                issue_t(it + 1, dv0, C::kOffDO, C::kColDP, 1);
+                mma_commit(BAR(kDPFull));
+                if (it + 2 < n_it) {
+                    if (!mbar_wait(BAR(kQFull + (it + 2) % S), ((it + 2) / S) & 1, abort_p, 57, p.status)) break;
+                    tc_fence_after();
+                    issue_t(it + 2, dk0, C::kOffQ, C::kColS, 0);  // after dV(it+1), which read P^T here
+                    mma_commit(BAR(kSFull));
+                }
+            } else {
+                mma_commit(BAR(kOReady));
+            }
+        }
+        // every issued MMA completes before TMEM is freed (after an abort, too)
+        mma_commit(BAR(kDrain));
+        mbar_drain(BAR(kDrain), 0, 62, p.status);
+    } else if (warp < kKqEwWarps) {
+        // ---------------------------------------------------------------- element-wise warps
+        // warp w: TMEM lanes 32 (w % 4) .. + 31 (its key rows of S^T / dP^T, its query rows of dQ),
+        // query columns (and dQ columns) of half w / 4
+        const int quad = warp & 3, half = warp >> 2;
+        const int krow = quad * 32 + lane;  // key row of S^T, dP^T and dS^T; query row of dQ
+        const int key = kt * C::kBK + krow;
+        const bool key_ok = key < p.Nkv;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t col_s = C::kColS + half * 64, col_dp = C::kColDP + half * 64;
+        float pf[64];
+        bool ok = true;
+        // a wait whose outcome is the same for the whole warp (the TMEM loads and stores after it
+        // are warp-collective): a warp gives up if any of its lanes did
+        auto ew_wait = [&](int idx, uint32_t parity, int site) {
+            return __all_sync(0xffffffffu, mbar_wait(BAR(idx), parity, abort_p, site, p.status));
+        };
+        // P = exp2(S' scale log2 e) of step j (S' = S - lse / scale), bf16 over S^T for dV
+        auto do_p = [&](int j) -> bool {
+            const int qt = qt_lo + j % nq;
+            if (!ew_wait(kSFull, j & 1, 63)) return false;
+            tc_fence_after();
+            uint32_t ra[32], rb[32];
+            tmem_ld32(lane_base + col_s, ra);
+            tmem_ld32(lane_base + col_s + 32, rb);
+            tmem_wait_ld();
+            const int q0 = qt * C::kBQ + half * 64;  // query of column 0
+            const bool need_mask = (p.causal && q0 + shift < kt * C::kBK + C::kBK - 1) || !key_ok;
+            const int qmin_ok = key_ok ? (p.causal ? key - shift - q0 : 0) : 64;  // first visible column
+            uint32_t pk[32];
+            const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+                const float2 x = mul2(make_float2(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]),
+                                                  __uint_as_float(e < 32 ? ra[e + 1] : rb[e - 31])),
+                                      c2);
+                pf[e] = ex2_approx(x.x);
+                pf[e + 1] = ex2_approx(x.y);
+                if (need_mask) {
+                    if (e < qmin_ok) pf[e] = 0.f;
+                    if (e + 1 < qmin_ok) pf[e + 1] = 0.f;
+                }
+                pk[e / 2] = pack_bf16(pf[e], pf[e + 1]);
+            }
+            tmem_st32(lane_base + col_s, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(kPReady));
+            return true;
+        };
+        // dS = P (dP - D) of step j (dP' = dP - D), bf16, as this thread's row of dS^T in shared memory
+        auto do_ds = [&](int j) -> bool {
+            if (!ew_wait(kDPFull, j & 1, 64)) return false;
+            tc_fence_after();
+            uint32_t ra[32], rb[32];
+            tmem_ld32(lane_base + col_dp, ra);
+            tmem_ld32(lane_base + col_dp + 32, rb);
+            tmem_wait_ld();
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+                const float2 ds = mul2(make_float2(pf[e], pf[e + 1]),
+                                       make_float2(__uint_as_float(e < 32 ? ra[e] : rb[e - 32]),
+                                                   __uint_as_float(e < 32 ? ra[e + 1] : rb[e - 31])));
+                pk[e / 2] = pack_bf16(ds.x, ds.y);
+            }
+            // at d = 128 dS^T goes over this step's dO tile: wait until dV(j), its last reader, is done
+            if (C::kDsInDo && !ew_wait(kDVDone, j & 1, 65)) return false;
+            // row krow, queries 64 half .. + 63: one 128-byte row of the 128-byte-swizzled K-major tile
+            uint8_t* row = smem + ds_off(j) + half * 16384 + krow * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<uint4*>(row + ((u ^ (krow & 7)) << 4)) =
+                    make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(BAR(kDSReady));
+            return true;
+        };
+        // dQ(j) from the dP^T columns (this warp's query rows, columns half * D/2 ..) into the accumulator
+        auto do_dq = [&](int j) -> bool {
+            if (!ew_wait(kDQFull, j & 1, 66)) return false;
+            tc_fence_after();
+            uint32_t ra[32], rb[32];
+            tmem_ld32(lane_base + C::kColDP + half * (D / 2), ra);
+            if constexpr (D == 128) tmem_ld32(lane_base + C::kColDP + half * (D / 2) + 32, rb);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(BAR(kDQFree));  // the values are in registers: dP^T(j+1) may overwrite them
+            const int hq = hk * p.g + j / nq;
+            const int qt = qt_lo + j % nq;
+            float* tile = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D;
+#pragma unroll
+            for (int e = 0; e < D / 8; ++e) {  // column group half * D/8 + e: columns 4 e .. of this half
+                const uint32_t* r = e < 8 ? &ra[4 * e] : &rb[4 * (e - 8)];
+                red_add_v4(tile + ((half * (D / 8) + e) * C::kBQ + krow) * 4, __uint_as_float(r[0]),
+                           __uint_as_float(r[1]), __uint_as_float(r[2]), __uint_as_float(r[3]));
+            }
+            return true;
+        };
+        if (n_it > 0) ok = do_p(0) && do_ds(0);
+        for (int it = 0; ok && it < n_it; ++it) {
+            if (it + 1 < n_it && !do_p(it + 1)) { ok = false; break; }
+            if (!do_dq(it)) { ok = false; break; }
+            if (it + 1 < n_it && !do_ds(it + 1)) { ok = false; break; }
+        }
+        if (ok && n_it > 0) ok = ew_wait(kOReady, 0, 67);
+        if (ok) {
+            // warps 0-3 write dV, warps 4-7 write dK (scale applied here)
+            tc_fence_after();
+            const bool valid = key < p.Nkv;
+            const TokOuter ka = split_pos(key, kv_outer, SPLIT ? p.split_np : 0, p.split_b);
+            const int64_t base = (int64_t)ka.outer * p.k_s_outer + (int64_t)hk * p.k_s_head + (int64_t)ka.tok * p.k_s_tok;
+            const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
+            const float mul = half == 0 ? 1.f : p.scale;
+            uint16_t* out16 = half == 0 ? p.dv : p.dk;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t r[32];
+                if (n_it > 0) {
+                    tmem_ld32(lane_base + col + cc * 32, r);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = 0u;
+                }
+                if (valid) store_row32(out16, nullptr, 0, base + cc * 32, r, mul);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kKqMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// The dQ accumulator to zero: 16-byte stores, grid-stride (n4 = float4 count).
+__global__ void __launch_bounds__(256) zero_f32x4_kernel(float4* dst, int64_t n4) {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) dst[i] = z;
+}
+
+// dQ = scale * accumulator, rounded to bf16: thread (tile, part, row) converts columns 32 part .. + 31
+// of one query row (reads of consecutive threads are consecutive 16-byte groups of the tile).
+template <int D, bool SPLIT>
+__global__ void __launch_bounds__(256) dq_store_kernel(const DevBwd p, int64_t n_threads) {
+    const int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (t >= n_threads) return;
+    constexpr int kParts = D / 32;
+    const int r = (int)(t % 128);
+    const int part = (int)((t / 128) % kParts);
+    const int64_t tile = t / (128 * kParts);  // z * (Npad / 128) + query tile
+    const int64_t tiles_per_z = p.Npad / 128;
+    const int z = (int)(tile / tiles_per_z);
+    const int n = (int)(tile % tiles_per_z) * 128 + r;
+    if (n >= p.N) return;
+    const float* src = p.dq_acc + tile * 128 * D;
+    uint32_t v[32];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const float4 x = *reinterpret_cast<const float4*>(src + ((part * 8 + g) * 128 + r) * 4);
+        v[4 * g] = __float_as_uint(x.x);
+        v[4 * g + 1] = __float_as_uint(x.y);
+        v[4 * g + 2] = __float_as_uint(x.z);
+        v[4 * g + 3] = __float_as_uint(x.w);
+    }
+    const int outer = z / p.Hq, head = z % p.Hq;
+    const TokOuter at = split_pos(n, outer, SPLIT ? p.split_np : 0, p.split_b);
+    const int64_t off = (int64_t)at.outer * p.q_s_outer + (int64_t)head * p.q_s_head + (int64_t)at.tok * p.q_s_tok +
+                        part * 32;
+    store_row32(p.dq, nullptr, 0, off, v, p.scale);
+}
+
 struct BwdMaps {
     CUtensorMap q, dout, k, v;
 };
@@ -912,6 +1375,7 @@ DevBwd dev_params(const BwdParams& b) {
     p.k_s_tok = b.k.s_tok;
     p.k_s_outer = b.k.s_outer;
     p.status = b.status;
+    p.dq_acc = b.dq_acc;
     return p;
 }
 
@@ -973,6 +1437,31 @@ cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int D, bool SPLIT>
+cudaError_t dkdvq_t(const BwdParams& b, cudaStream_t stream) {
+    if (!b.dq_acc || !b.dq) return cudaErrorInvalidValue;
+    BwdMaps m;
+    if (!make_bwd_maps<D>(b, KqCfg<D>::kBQ, &m)) return cudaErrorInvalidValue;
+    auto kern = dkdvq_kernel<D, SPLIT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, KqCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t n_kt = (kv_len_of(b) + 127) / 128;
+    const int64_t grid = n_kt * b.n_outer * (b.q.n_head / b.g);
+    if (grid == 0) return cudaSuccess;
+    kern<<<(unsigned)grid, kKqThreads, KqCfg<D>::kSmemBytes, stream>>>(m.q, m.dout, m.k, m.v, dev_params(b));
+    return cudaGetLastError();
+}
+
+template <int D, bool SPLIT>
+cudaError_t dq_store_t(const BwdParams& b, cudaStream_t stream) {
+    if (!b.dq_acc || !b.dq) return cudaErrorInvalidValue;
+    const DevBwd p = dev_params(b);
+    const int64_t n_threads = (int64_t)b.n_z * p.Npad * (D / 32);
+    if (n_threads == 0) return cudaSuccess;
+    dq_store_kernel<D, SPLIT><<<(unsigned)((n_threads + 255) / 256), 256, 0, stream>>>(p, n_threads);
+    return cudaGetLastError();
+}
+
 // each pass in two forms: the sequence-sharded in-place addressing (split_np > 0) or not
 template <template <int, bool> class F>
 cudaError_t dispatch(const BwdParams& b, cudaStream_t stream) {
@@ -993,11 +1482,29 @@ template <int D, bool S>
 struct DqF {
     static cudaError_t run(const BwdParams& b, cudaStream_t s) { return dq_t<D, S>(b, s); }
 };
+template <int D, bool S>
+struct DkdvqF {
+    static cudaError_t run(const BwdParams& b, cudaStream_t s) { return dkdvq_t<D, S>(b, s); }
+};
+template <int D, bool S>
+struct DqStoreF {
+    static cudaError_t run(const BwdParams& b, cudaStream_t s) { return dq_store_t<D, S>(b, s); }
+};
 
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdParams& b, cudaStream_t stream) { return dispatch<PreF>(b, stream); }
 cudaError_t launch_bwd_dkdv(const BwdParams& b, cudaStream_t stream) { return dispatch<DkdvF>(b, stream); }
 cudaError_t launch_bwd_dq(const BwdParams& b, cudaStream_t stream) { return dispatch<DqF>(b, stream); }
+cudaError_t launch_bwd_dq_zero(const BwdParams& b, cudaStream_t stream) {
+    if (!b.dq_acc) return cudaErrorInvalidValue;
+    const int64_t n4 = (int64_t)b.n_z * npad_of(b) * b.d / 4;  // 128-row tiles of d values: a multiple of 4
+    if (n4 == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, 152 * 8);
+    zero_f32x4_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<float4*>(b.dq_acc), n4);
+    return cudaGetLastError();
+}
+cudaError_t launch_bwd_dkdvq(const BwdParams& b, cudaStream_t stream) { return dispatch<DkdvqF>(b, stream); }
+cudaError_t launch_bwd_dq_store(const BwdParams& b, cudaStream_t stream) { return dispatch<DqStoreF>(b, stream); }
 
 }  // namespace usp

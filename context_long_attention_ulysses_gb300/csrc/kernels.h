@@ -103,12 +103,23 @@ struct BwdParams {
     int split_np, split_b;
     float scale;
     int* status;
+    // one-pass backward only: float32 dQ accumulator, n_z * Npad rows of d values in 128-row tiles,
+    // each tile stored as [d/4 column groups][128 rows][4] (so that a warp's 32 rows of one group
+    // are 512 contiguous bytes); null for the three-pass backward
+    float* dq_acc;
 };
 // The three passes, in this order: the workspace rows (launch_bwd_pre covers
 // all n_z rows), then dK/dV, then dQ (these two cover the launch's outer indices).
 cudaError_t launch_bwd_pre(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream);
+// The one-pass backward (bf16 results only), in this order: the dQ accumulator zeroed
+// (launch_bwd_dq_zero) and the workspace rows (launch_bwd_pre), dK, dV and the dQ partials of
+// every block pair (launch_bwd_dkdvq), then dQ = scale * accumulator rounded to bf16
+// (launch_bwd_dq_store).
+cudaError_t launch_bwd_dq_zero(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dkdvq(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq_store(const BwdParams& p, cudaStream_t stream);
 
 // ---- ring attention merge (ring.cu)
 cudaError_t launch_lse_merge(int64_t rows, int d, const float* o_a, const float* lse_a, const float* o_b,

@@ -1,12 +1,13 @@
 // Attention backward for callers that cannot allocate device memory.
 //
-// usp_attn_bwd needs a caller-provided workspace (40 bytes per query row,
-// rows padded to 128-row tiles).  Some callers cannot obtain one: code running inside a
+// The backward needs a caller-provided workspace: the deterministic
+// three-pass backward (usp_attn_bwd_deterministic) 40 bytes per query row,
+// rows padded to 128-row tiles.  Some callers cannot obtain one: code running inside a
 // framework that owns every device allocation and forbids raw cudaMalloc,
 // plugins loaded into a host process that has no allocator to hand them, or
 // code that must not touch the allocator at all once set up.  This file gives
-// them usp_attn_bwd_noalloc, which uses a fixed scratch array compiled into
-// the library instead.
+// them usp_attn_bwd_noalloc, the deterministic backward with a fixed scratch
+// array compiled into the library as its workspace.
 //
 // The scratch is a file-scope __device__ array of USP_NOALLOC_SCRATCH_BYTES.
 // Every GPU that loads the library holds it until the process exits.  Host
@@ -55,7 +56,7 @@ extern "C" usp_status usp_attn_bwd_noalloc(const usp_problem* p, const void* q, 
     // not support, or one the scratch cannot hold, is refused with nothing looked up or enqueued.
     usp_status st = usp::attn_bwd_check(p, q, k, v, o, lse, dout, dq, dk, dv);
     if (st != USP_OK) return st;
-    const size_t need = usp_attn_bwd_workspace_size(p);
+    const size_t need = usp_attn_bwd_deterministic_workspace_size(p);
     if (need == 0) return USP_OK;  // an empty problem: nothing to do
     if (need > kScratchBytes) return USP_ERR_WORKSPACE;
     void* scratch = nullptr;
@@ -63,5 +64,5 @@ extern "C" usp_status usp_attn_bwd_noalloc(const usp_problem* p, const void* q, 
     if (st != USP_OK) return st;
     // The backward's first pass rewrites every scratch entry the later passes
     // read, so the previous call's contents never matter.
-    return usp_attn_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, scratch, kScratchBytes, stream);
+    return usp_attn_bwd_deterministic(p, q, k, v, o, lse, dout, dq, dk, dv, scratch, kScratchBytes, stream);
 }

@@ -121,10 +121,11 @@ usp_status usp_a2a_head2seq(const usp_problem* p, int Hx, const void* src, void*
 usp_status usp_attn_fwd(const usp_problem* p, const void* q, const void* k, const void* v, void* o,
                         float* lse, usp_stream stream);
 
-/* Bytes of workspace usp_attn_bwd needs: linear in N, never quadratic: 40
- * bytes per query row, rows padded to 128-row tiles (D_i and lse_i*log2(e)
+/* Bytes of workspace usp_attn_bwd needs: linear in N, never quadratic: per
+ * query row, rows padded to 128-row tiles, 40 bytes (D_i and lse_i*log2(e)
  * as float32, and -lse_i/scale and -D_i each as three bf16 numbers in a
- * 16-byte row).  Returns 0 for an invalid problem. */
+ * 16-byte row) plus the float32 dQ accumulator (4*d bytes).  Returns 0 for an
+ * invalid problem. */
 size_t usp_attn_bwd_workspace_size(const usp_problem* p);
 
 /* Attention backward on head-sharded buffers (the backward of the glossary
@@ -136,21 +137,44 @@ size_t usp_attn_bwd_workspace_size(const usp_problem* p);
  * q, o, dout, dq as q above; k, v, dk, dv as k above; lse from usp_attn_fwd.
  * ws: device workspace of at least usp_attn_bwd_workspace_size(p) bytes,
  * 256-byte aligned; its contents on entry do not matter.  dtype BF16 only
- * (USP_ERR_UNSUPPORTED for F32). */
+ * (USP_ERR_UNSUPPORTED for F32).
+ * One pass over the visible block pairs computes S and dP once per pair: dK
+ * and dV accumulate in fixed order (bit-reproducible); each pair's part of
+ * dQ is added into a float32 accumulator in the workspace by atomic
+ * reductions, whose order varies from run to run, so dQ can differ between
+ * runs in its last bf16 bit.  usp_attn_bwd_deterministic gives bit-
+ * reproducible results. */
 usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
                         const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                         size_t ws_bytes, usp_stream stream);
 
+/* Bytes of workspace usp_attn_bwd_deterministic needs: 40 bytes per query
+ * row, rows padded to 128-row tiles (the rows of usp_attn_bwd's workspace,
+ * without the dQ accumulator).  Returns 0 for an invalid problem. */
+size_t usp_attn_bwd_deterministic_workspace_size(const usp_problem* p);
+
+/* usp_attn_bwd with bit-reproducible results: the same operation, layouts and
+ * checks, computed in three passes without atomics (the softmax statistics,
+ * then dK and dV per key tile, then dQ per query tile, which computes S and
+ * dP a second time).  dK and dV equal usp_attn_bwd's bit for bit; dQ agrees
+ * to rounding.  ws: at least usp_attn_bwd_deterministic_workspace_size(p)
+ * bytes, 256-byte aligned. */
+usp_status usp_attn_bwd_deterministic(const usp_problem* p, const void* q, const void* k, const void* v,
+                                      const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                                      void* dv, void* ws, size_t ws_bytes, usp_stream stream);
+
 /* Size of the scratch array built into the library for
  * usp_attn_bwd_noalloc: 64 MiB, enough for B*Hq*roundup(N,128) <= 1.6 Mi
- * query rows at 40 bytes each (e.g. 32 heads of 49 152 tokens). */
+ * query rows at 40 bytes each (e.g. 32 heads of 49 152 tokens): the workspace
+ * of usp_attn_bwd_deterministic. */
 #define USP_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /* usp_attn_bwd for callers that cannot allocate device memory -- code inside
  * a framework that owns every device allocation, plugins handed no
  * allocator, or code that must not call the allocator once running.  The
  * pages have no counterpart to this entry point; it exists for such callers.
- * Same arguments, layouts and results as usp_attn_bwd, minus the workspace:
+ * Same arguments, layouts and results as usp_attn_bwd_deterministic (whose
+ * small workspace suits a fixed array), minus the workspace:
  * the workspace is a file-scope device array of USP_NOALLOC_SCRATCH_BYTES
  * inside the library, held on every GPU that loads it until the process
  * exits.  Nothing is allocated or freed by the call.
@@ -163,8 +187,8 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
  *  - Checks: every argument check of usp_attn_bwd (sizes, d, dtype,
  *    pointers), then the size limit, come before any CUDA call.  Problems
  *    needing more than USP_NOALLOC_SCRATCH_BYTES
- *    (usp_attn_bwd_workspace_size) return USP_ERR_WORKSPACE with nothing
- *    enqueued.
+ *    (usp_attn_bwd_deterministic_workspace_size) return USP_ERR_WORKSPACE
+ *    with nothing enqueued.
  *  - Sharing: every call on a device uses the same array, and the array keeps
  *    the last call's contents (each call rewrites every entry it reads before
  *    reading it).  Calls that can overlap on the GPU -- on different streams,
@@ -295,8 +319,10 @@ usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* 
  * every result row addresses token n of a head as row n mod (N/P) of shard
  * n div (N/P), so no remap runs and no head-sharded copy exists.  Results are
  * those of usp_a2a_seq2head -> usp_attn_fwd / usp_attn_bwd -> usp_a2a_head2seq,
- * bit for bit (the same per-head work, tile for tile); only the LSE layout
- * differs: float32 [P][B][N/P][Hq], as in ring mode.
+ * bit for bit (the same per-head work, tile for tile), except dQ, whose
+ * float32 accumulation order varies from run to run in both (see
+ * usp_attn_bwd); only the LSE layout differs: float32 [P][B][N/P][Hq], as in
+ * ring mode.
  * Preconditions as usp_attn_fwd (Hq % P = Hkv % P = 0, dtype BF16, d in
  * {64, 128}) plus (N/P) % 128 == 0: a 128-row tile never straddles two shards
  * (USP_ERR_UNSUPPORTED otherwise). */
@@ -307,9 +333,10 @@ usp_status usp_fused_attn_fwd(const usp_problem* p, const void* q, const void* k
  * usp_attn_bwd_workspace_size); 0 for an invalid problem. */
 size_t usp_fused_attn_bwd_workspace_size(const usp_problem* p);
 
-/* Backward of usp_fused_attn_fwd: q, k, v, o, dout, dq, dk, dv sequence-
- * sharded, lse as the forward wrote it.  ws: at least
- * usp_fused_attn_bwd_workspace_size(p) bytes, 256-byte aligned. */
+/* Backward of usp_fused_attn_fwd (the one-pass backward of usp_attn_bwd):
+ * q, k, v, o, dout, dq, dk, dv sequence-sharded, lse as the forward wrote it.
+ * ws: at least usp_fused_attn_bwd_workspace_size(p) bytes, 256-byte
+ * aligned. */
 usp_status usp_fused_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
                               const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                               size_t ws_bytes, usp_stream stream);

@@ -87,6 +87,18 @@ def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
     return float(np.linalg.norm((a - b).ravel()) / (den if den > 0 else 1.0))
 
 
+def bf16_ulp_diff(got: np.ndarray, want: np.ndarray) -> float:
+    """Largest |got - want| over the elements, in units of the bf16 spacing (2^(e - 7) for
+    2^e <= |x| < 2^(e+1)) at the larger of the two magnitudes; bf16 bit arrays in.  Two sums
+    of the same float32 terms in different orders, each rounded once to bf16, differ by at
+    most one such unit."""
+    a, b = f64(got), f64(want)
+    mag = np.maximum(np.abs(a), np.abs(b))
+    tiny = 2.0 ** -126
+    ulp = np.exp2(np.floor(np.log2(np.maximum(mag, tiny))) - 7)
+    return float(np.max(np.abs(a - b) / ulp)) if a.size else 0.0
+
+
 def max_abs(a, b) -> float:
     return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64)))) if np.size(a) else 0.0
 

@@ -150,10 +150,15 @@ def test_empty_problems_enqueue_nothing(lib):
 
 def test_workspaces_are_linear_in_sequence_length(lib):
     for N in (1024, 4096, 131072):
-        a = usp.usp_attn_bwd_workspace_size(_p(N=N, Hq=32, Hkv=8, d=128, P=8))
-        b = usp.usp_attn_bwd_workspace_size(_p(N=2 * N, Hq=32, Hkv=8, d=128, P=8))
+        a = usp.usp_attn_bwd_deterministic_workspace_size(_p(N=N, Hq=32, Hkv=8, d=128, P=8))
+        b = usp.usp_attn_bwd_deterministic_workspace_size(_p(N=2 * N, Hq=32, Hkv=8, d=128, P=8))
         assert b == 2 * a
         assert a == 40 * 32 * N  # per query row: D_i, lse_i*log2(e) (float32) and two 16-byte bf16 split rows
+        # the one-pass backward adds a float32 dQ accumulator row of d values per query row
+        a1 = usp.usp_attn_bwd_workspace_size(_p(N=N, Hq=32, Hkv=8, d=128, P=8))
+        assert a1 == (40 + 4 * 128) * 32 * N
+        assert usp.usp_attn_bwd_workspace_size(_p(N=2 * N, Hq=32, Hkv=8, d=128, P=8)) == 2 * a1
+        assert usp.usp_fused_attn_bwd_workspace_size(_p(N=N, Hq=32, Hkv=8, d=128, P=8)) == a1
         r1 = usp.usp_ring_workspace_size(_p(N=N, Hq=32, Hkv=32, d=128, P=8))
         r2 = usp.usp_ring_workspace_size(_p(N=2 * N, Hq=32, Hkv=32, d=128, P=8))
         assert r2 == 2 * r1
@@ -223,7 +228,7 @@ def test_zigzag_argument_errors(lib):
 def test_fused_argument_errors(lib):
     p = _p()                                                   # N/P = 128: one tile per shard
     bws = usp.usp_fused_attn_bwd_workspace_size(p)
-    assert bws == usp.usp_attn_bwd_workspace_size(p) == 40 * p.B * p.Hq * p.N
+    assert bws == usp.usp_attn_bwd_workspace_size(p) == (40 + 4 * p.d) * p.B * p.Hq * p.N  # rows + dQ accumulator
     for kw, code in ((dict(N=200), _lib.USP_ERR_UNSUPPORTED),  # shards of 100 tokens: tiles would straddle
                      (dict(N=384), _lib.USP_ERR_UNSUPPORTED),  # shards of 192 tokens
                      (dict(Hq=3, Hkv=3), _lib.USP_ERR_INVALID_ARG),   # heads are split over the ranks

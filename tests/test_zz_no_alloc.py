@@ -2,10 +2,10 @@
 
 usp_attn_bwd_noalloc serves code that is not allowed to call cudaMalloc (for
 example inside a framework that owns all device memory): it runs the same
-backward as usp_attn_bwd but keeps its workspace in a fixed array built into
-the library.  These tests call it through the C ABI and compare it with the
-workspace-taking entry point on the same inputs, bit for bit (the backward is
-deterministic), on two calls in a row, after a call on a larger, different
+deterministic backward as usp_attn_bwd_deterministic but keeps its workspace
+in a fixed array built into the library.  These tests call it through the C
+ABI and compare it with the workspace-taking entry point on the same inputs,
+bit for bit, on two calls in a row, after a call on a larger, different
 problem has left its own rows (padding rows included) in the shared array.
 This file is collected last on purpose.
 """
@@ -25,7 +25,7 @@ def usp():
 def test_rejects_problems_larger_than_the_scratch(usp):
     # needs 40 bytes * 32 heads * 524288 rows = 640 MiB > the built-in 64 MiB; refused before any CUDA call
     p = usp.Problem(B=1, Hq=32, Hkv=8, N=524288, d=128, P=8)
-    assert usp.usp_attn_bwd_workspace_size(p) > usp.NOALLOC_SCRATCH_BYTES
+    assert usp.usp_attn_bwd_deterministic_workspace_size(p) > usp.NOALLOC_SCRATCH_BYTES
     fake = 1 << 20
     with pytest.raises(usp.UspError) as e:
         usp.usp_attn_bwd_noalloc(p, *([fake] * 9))
@@ -80,9 +80,9 @@ def test_noalloc_backward_matches_workspace_backward(usp):
     p, ins = _problem_inputs(usp, 1, 8, 2, 1000, 128, 2, seed=0)
     qh, kh, vh = ins[:3]
     # reference: the entry point that takes a caller-allocated workspace
-    ws = torch.empty(usp.usp_attn_bwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(usp.usp_attn_bwd_deterministic_workspace_size(p), dtype=torch.uint8, device="cuda")
     ref = [torch.empty_like(qh), torch.empty_like(kh), torch.empty_like(vh)]
-    usp.usp_attn_bwd(p, *ins, *ref, ws)
+    usp.usp_attn_bwd_deterministic(p, *ins, *ref, ws)
     torch.cuda.synchronize()
     want = [to_host(t).tobytes() for t in ref]
 
