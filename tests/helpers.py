@@ -87,16 +87,22 @@ def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
     return float(np.linalg.norm((a - b).ravel()) / (den if den > 0 else 1.0))
 
 
-def bf16_ulp_diff(got: np.ndarray, want: np.ndarray) -> float:
+def bf16_ulp_diff(got: np.ndarray, want: np.ndarray, floor: float = 2.0 ** -16) -> float:
     """Largest |got - want| over the elements, in units of the bf16 spacing (2^(e - 7) for
-    2^e <= |x| < 2^(e+1)) at the larger of the two magnitudes; bf16 bit arrays in.  Two sums
-    of the same float32 terms in different orders, each rounded once to bf16, differ by at
-    most one such unit."""
+    2^e <= |x| < 2^(e+1)) at the larger of the two magnitudes, after allowing an absolute
+    `floor` * max|want|; bf16 bit arrays in.  Two float32 sums of the same terms in different
+    orders, each rounded once to bf16, differ by at most one unit, except where the sum is far
+    smaller than its terms (a row of dQ sums terms whose total nearly cancels): there the
+    float32 rounding of the terms, about 2^-24 of their size, can exceed a unit of the tiny
+    result, and the floor (2^-16 of the largest element, 2^8 times that rounding) covers it."""
     a, b = f64(got), f64(want)
+    if not a.size:
+        return 0.0
     mag = np.maximum(np.abs(a), np.abs(b))
     tiny = 2.0 ** -126
     ulp = np.exp2(np.floor(np.log2(np.maximum(mag, tiny))) - 7)
-    return float(np.max(np.abs(a - b) / ulp)) if a.size else 0.0
+    atol = floor * float(np.max(np.abs(b)))
+    return float(np.max(np.maximum(np.abs(a - b) - atol, 0.0) / ulp))
 
 
 def max_abs(a, b) -> float:
