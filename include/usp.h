@@ -157,8 +157,9 @@ size_t usp_attn_bwd_deterministic_workspace_size(const usp_problem* p);
  * checks, computed in three passes without atomics (the softmax statistics,
  * then dK and dV per key tile, then dQ per query tile, which computes S and
  * dP a second time).  dK and dV equal usp_attn_bwd's bit for bit; dQ agrees
- * to rounding.  ws: at least usp_attn_bwd_deterministic_workspace_size(p)
- * bytes, 256-byte aligned. */
+ * within the rounding of dS to bf16 (the dQ pass forms dS its own way).
+ * ws: at least usp_attn_bwd_deterministic_workspace_size(p) bytes, 256-byte
+ * aligned. */
 usp_status usp_attn_bwd_deterministic(const usp_problem* p, const void* q, const void* k, const void* v,
                                       const void* o, const float* lse, const void* dout, void* dq, void* dk,
                                       void* dv, void* ws, size_t ws_bytes, usp_stream stream);

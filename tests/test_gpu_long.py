@@ -90,16 +90,17 @@ def test_ulysses_long_context(usp, orc, B, Hq, Hkv, N, d, P, kv_groups):
     lse_u = saved["lse"].permute(1, 0, 2, 3).reshape(B, Hq, N)
     assert torch.equal(lse_f.permute(1, 3, 0, 2).reshape(B, Hq, N).view(torch.int32), lse_u.view(torch.int32))
     del o_f, lse_f, grads_f, lse_u
-    # the three-pass (deterministic) backward at full size: dK and dV bit for bit, dQ to two units
+    # the three-pass (deterministic) backward at full size: dK and dV bit for bit, dQ within a tenth
+    # of the gradient tolerance (its dQ pass rounds dS its own way)
     grads_3 = usp.ulysses_attention_bwd(p, saved, dos, deterministic=True)
     torch.cuda.synchronize()
     assert usp.usp_device_status() == 0
     for got, want in zip(grads_3[1:], (dk_s, dv_s)):
         assert torch.equal(got.view(torch.int16), want.view(torch.int16))
-    ulps = bf16_ulp_diff(to_host(grads_3[0]), to_host(dq_s))
+    d13 = float((grads_3[0].float() - dq_s.float()).norm() / dq_s.float().norm())
     if VERBOSE:
-        print(f"\n[N={N}] one-pass vs three-pass dQ: {ulps:.2f} bf16 units at most")
-    assert ulps <= 2.0
+        print(f"\n[N={N}] one-pass vs three-pass dQ: relative Frobenius {d13:.3e}")
+    assert d13 < 0.1 * TOL_BF16_GRAD_RELFRO
     del grads_3
 
     # all-to-all: the oracle's index map, bit for bit

@@ -366,9 +366,12 @@ def test_fused_equals_remapped(usp, B, Hq, Hkv, N, d, P, causal):
     (1, 16, 4, 2048, 64, 4, True)])    # GQA at d = 64, 16 query tiles
 def test_one_pass_backward_matches_three_pass(usp, orc, B, Hq, Hkv, N, d, P, causal):
     """usp_attn_bwd (S and dP once per block pair, dQ partials added into a float32 accumulator)
-    against usp_attn_bwd_deterministic (dK/dV pass, then a dQ pass): dK and dV bit for bit, dQ to
-    two bf16 units (float32 sums of the same products in other orders; the three-pass dQ adds
-    every key tile in one TMEM accumulator, the one-pass dQ 128 keys at a time)."""
+    against usp_attn_bwd_deterministic (dK/dV pass, then a dQ pass): dK and dV bit for bit; dQ
+    within a tenth of the gradient tolerance (relative Frobenius), and each against the oracle on
+    every element.  The dQ pass of the three-pass backward recomputes dS with its own rounding
+    (lse and D subtracted in registers instead of inside the product), so its bf16 dS can differ
+    from the one dK uses in the last bit: on entries of dQ whose terms nearly cancel, the two dQ
+    then differ by more than a unit of the (small) result."""
     import torch
     p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P, causal=causal)
     q, k, v, dO = gen((B, Hq, N, d), 0), gen((B, Hkv, N, d), 1), gen((B, Hkv, N, d), 2), gen((B, Hq, N, d), 3)
@@ -386,10 +389,12 @@ def test_one_pass_backward_matches_three_pass(usp, orc, B, Hq, Hkv, N, d, P, cau
     _status_ok(usp)
     assert to_host(one[1]).tobytes() == to_host(three[1]).tobytes()
     assert to_host(one[2]).tobytes() == to_host(three[2]).tobytes()
-    assert bf16_ulp_diff(to_host(one[0]), to_host(three[0])) <= 2.0
-    # and the one-pass dQ against the oracle, every element
+    dq1, dq3 = f64(from_head(to_host(one[0]))), f64(from_head(to_host(three[0])))
+    assert rel_fro(dq1, dq3) < 0.1 * TOL_BF16_GRAD_RELFRO
+    # each dQ against the oracle, every element
     ref_dq, _, _, _, _ = orc.attn_bwd_full(q, k, v, dO, causal=causal)
-    assert rel_fro(f64(from_head(to_host(one[0]))), ref_dq) < TOL_BF16_GRAD_RELFRO
+    assert rel_fro(dq1, ref_dq) < TOL_BF16_GRAD_RELFRO
+    assert rel_fro(dq3, ref_dq) < TOL_BF16_GRAD_RELFRO
 
 
 def test_fused_against_oracle_mean_square_loss(usp, orc):
