@@ -425,20 +425,22 @@ static cudaError_t ring_fwd_schedule(FwdParams f, int n_groups, int per_member, 
 // pair (i, (i - t) mod n_groups) -- dK, dV travel with the KV block, dQ stays with the queries,
 // masked only on the diagonal (t = 0).  Every block receives its first contribution at t = 0, so
 // later steps add.  The accumulators are rounded to bf16 once.
-static cudaError_t ring_bwd_schedule(BwdParams b, int n_groups, int per_member, bool causal, size_t q_elems,
-                                     size_t k_elems, void* dq, void* dk, void* dv, const char* name_dkdv,
-                                     const char* name_dq, cudaStream_t s) {
-    cudaError_t e = cudaSuccess;
+// Every step runs the one-pass kernel: its dQ partials go into the float32 dQ accumulator b.dq_acc
+// (zeroed first, rounded to bf16 into dq at the end), its dK and dV into the float32 accumulators
+// b.dk_f32 and b.dv_f32 (written at t = 0, added to after).
+static cudaError_t ring_bwd_schedule(BwdParams b, int n_groups, int per_member, bool causal, size_t k_elems,
+                                     void* dq, void* dk, void* dv, const char* name_step, cudaStream_t s) {
+    cudaError_t e = traced("ring_bwd_dq_zero", s, [&] { return launch_bwd_dq_zero(b, s); });
     for (int t = 0; e == cudaSuccess && t < n_groups; ++t) {
         b.ring_t = t;
         b.ring_i0 = causal ? t : 0;
         b.n_outer = (causal ? n_groups - t : n_groups) * per_member;
         b.causal = (causal && t == 0) ? 1 : 0;
         b.accumulate = t > 0 ? 1 : 0;
-        e = traced(name_dkdv, s, [&] { return launch_bwd_dkdv(b, s); });
-        if (e == cudaSuccess) e = traced(name_dq, s, [&] { return launch_bwd_dq(b, s); });
+        e = traced(name_step, s, [&] { return launch_bwd_dkdvq(b, s); });
     }
-    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(b.dq_f32, dq, (int64_t)q_elems, s); });
+    b.dq = dq;
+    if (e == cudaSuccess) e = traced("ring_bwd_dq_store", s, [&] { return launch_bwd_dq_store(b, s); });
     if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(b.dk_f32, dk, (int64_t)k_elems, s); });
     if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(b.dv_f32, dv, (int64_t)k_elems, s); });
     return e;
@@ -508,7 +510,8 @@ usp_status usp_ring_attn_fwd(const usp_problem* p, const void* q, const void* k,
 
 // Ring backward workspace: the backward rows (40 bytes per padded query row
 // of every rank and head: D, lse*log2(e), -lse/scale and -D as bf16 splits),
-// then float32 accumulators for dQ, dK and dV in sequence-sharded order.
+// the float32 dQ accumulator (d values per padded row, in 128-row tiles), then
+// float32 accumulators for dK and dV in sequence-sharded order.
 static size_t ring_bwd_rows(const usp_problem* p) {
     const size_t npad = ((size_t)(p->N / p->P) + 127) / 128 * 128;
     return (size_t)p->P * p->B * p->Hq * npad;
@@ -516,8 +519,8 @@ static size_t ring_bwd_rows(const usp_problem* p) {
 
 size_t usp_ring_bwd_workspace_size(const usp_problem* p) {
     if (check_problem(p, false) != USP_OK) return 0;
-    const size_t q_elems = (size_t)p->B * p->N * p->Hq * p->d, k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
-    return ring_part(ring_bwd_rows(p) * 40) + ring_part(q_elems * 4) + 2 * ring_part(k_elems * 4);
+    const size_t k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
+    return ring_part(ring_bwd_rows(p) * 40) + ring_part(ring_bwd_rows(p) * p->d * 4) + 2 * ring_part(k_elems * 4);
 }
 
 usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k, const void* v, const void* o,
@@ -540,10 +543,10 @@ usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k,
 
     const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d;
     const int Np = p->N / P;
-    const size_t q_elems = (size_t)B * p->N * Hq * d, k_elems = (size_t)B * p->N * Hkv * d;
+    const size_t k_elems = (size_t)B * p->N * Hkv * d;
     char* w = static_cast<char*>(ws);
     float* acc_dq = reinterpret_cast<float*>(w + ring_part(ring_bwd_rows(p) * 40));
-    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(q_elems * 4));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(ring_bwd_rows(p) * d * 4));
     float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(k_elems * 4));
 
     BwdParams b{};
@@ -559,7 +562,7 @@ usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k,
     b.l_s_outer = (int64_t)Np * Hq;
     b.ws = reinterpret_cast<float*>(w);
     b.n_z = P * B * Hq;
-    b.dq_f32 = acc_dq;
+    b.dq_acc = acc_dq;
     b.dk_f32 = acc_dk;
     b.dv_f32 = acc_dv;
     b.d = d;
@@ -571,8 +574,7 @@ usp_status usp_ring_attn_bwd(const usp_problem* p, const void* q, const void* k,
 
     // D and the lse rows of every rank (they use the final O and the merged LSE)
     cudaError_t e = traced("ring_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    if (e == cudaSuccess)
-        e = ring_bwd_schedule(b, P, B, p->causal != 0, q_elems, k_elems, dq, dk, dv, "ring_bwd_dkdv", "ring_bwd_dq", s);
+    if (e == cudaSuccess) e = ring_bwd_schedule(b, P, B, p->causal != 0, k_elems, dq, dk, dv, "ring_bwd_dkdvq", s);
     return cuda_status(e);
 }
 
@@ -589,7 +591,8 @@ size_t usp_allgather_workspace_size(const usp_problem* p) {
 
 size_t usp_allgather_bwd_workspace_size(const usp_problem* p) {
     if (check_problem(p, false) != USP_OK) return 0;
-    return 2 * ring_part(gathered_bytes(p)) + ring_part(ring_bwd_rows(p) * 40) + 2 * ring_part(gathered_bytes(p) * 2);
+    return 2 * ring_part(gathered_bytes(p)) + ring_part(ring_bwd_rows(p) * 40) + ring_part(ring_bwd_rows(p) * p->d * 4) +
+           2 * ring_part(gathered_bytes(p) * 2);
 }
 
 static usp_status allgather_checks(const usp_problem* p, std::initializer_list<const void*> ptrs, const void* ws) {
@@ -681,7 +684,8 @@ usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const voi
     void* kg = w;
     void* vg = w + ring_part(gathered_bytes(p));
     float* rows = reinterpret_cast<float*>(w + 2 * ring_part(gathered_bytes(p)));
-    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(rows) + ring_part(ring_bwd_rows(p) * 40));
+    float* acc_dq = reinterpret_cast<float*>(reinterpret_cast<char*>(rows) + ring_part(ring_bwd_rows(p) * 40));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(ring_bwd_rows(p) * d * 4));
     float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(gathered_bytes(p) * 2));
     if (gather_kv(p, k, v, kg, vg, s) != cudaSuccess) return USP_ERR_CUDA;
 
@@ -698,7 +702,8 @@ usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const voi
     b.l_s_outer = (int64_t)Np * Hq;
     b.ws = rows;
     b.n_z = P * B * Hq;
-    b.dq = dq;  // dQ_i is complete after one pass of rank i over the gathered keys: bf16 directly
+    b.dq = dq;
+    b.dq_acc = acc_dq;
     b.dk_f32 = acc_dk;
     b.dv_f32 = acc_dv;
     b.d = d;
@@ -712,17 +717,19 @@ usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const voi
     b.status = sp;
 
     cudaError_t e = traced("allgather_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    b.ring_i0 = 0;
-    b.n_outer = P * B;
-    if (e == cudaSuccess) e = traced("allgather_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
+    if (e == cudaSuccess) e = traced("allgather_bwd_dq_zero", s, [&] { return launch_bwd_dq_zero(b, s); });
     // dK, dV: rank i's partial over the gathered keys, summed over the ranks in float32 (the
-    // reduce part of a reduce-scatter), one launch per rank in rank order
+    // reduce part of a reduce-scatter), one launch per rank in rank order; each launch also adds
+    // rank i's dQ partials (dQ_i is complete after rank i's launch)
     for (int i = 0; e == cudaSuccess && i < P; ++i) {
         b.ring_i0 = i;
         b.n_outer = B;
         b.accumulate = i > 0 ? 1 : 0;
-        e = traced("allgather_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+        e = traced("allgather_bwd_dkdvq", s, [&] { return launch_bwd_dkdvq(b, s); });
     }
+    b.ring_i0 = 0;
+    b.n_outer = P * B;
+    if (e == cudaSuccess) e = traced("allgather_bwd_dq_store", s, [&] { return launch_bwd_dq_store(b, s); });
     // the scatter part: rank j keeps the rows of its own shard, rounded to bf16
     const int64_t chunk = (int64_t)Np * Hkv * d;
     for (int j = 0; e == cudaSuccess && j < P; ++j)
@@ -795,8 +802,8 @@ size_t usp_zigzag_workspace_size(const usp_problem* p) {
 
 size_t usp_zigzag_bwd_workspace_size(const usp_problem* p) {
     if (zz_check(p) != USP_OK) return 0;
-    const size_t q_elems = (size_t)p->B * p->N * p->Hq * p->d, k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
-    return ring_part(zz_rows(p) * 40) + ring_part(q_elems * 4) + 2 * ring_part(k_elems * 4);
+    const size_t k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
+    return ring_part(zz_rows(p) * 40) + ring_part(zz_rows(p) * p->d * 4) + 2 * ring_part(k_elems * 4);
 }
 
 static usp_status zz_common_checks(const usp_problem* p, std::initializer_list<const void*> ptrs, const void* ws) {
@@ -881,10 +888,10 @@ usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int P = p->P, B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d;
     const int c = p->N / (2 * P);
-    const size_t q_elems = (size_t)B * p->N * Hq * d, k_elems = (size_t)B * p->N * Hkv * d;
+    const size_t k_elems = (size_t)B * p->N * Hkv * d;
     char* w = static_cast<char*>(ws);
     float* acc_dq = reinterpret_cast<float*>(w + ring_part(zz_rows(p) * 40));
-    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(q_elems * 4));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(zz_rows(p) * d * 4));
     float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(k_elems * 4));
 
     BwdParams b{};
@@ -900,7 +907,7 @@ usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* 
     b.l_s_outer = (int64_t)c * Hq;
     b.ws = reinterpret_cast<float*>(w);
     b.n_z = 2 * P * B * Hq;
-    b.dq_f32 = acc_dq;
+    b.dq_acc = acc_dq;
     b.dk_f32 = acc_dk;
     b.dv_f32 = acc_dv;
     b.d = d;
@@ -914,25 +921,22 @@ usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* 
     b.status = sp;
 
     cudaError_t e = traced("zigzag_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
+    if (e == cudaSuccess) e = traced("zigzag_bwd_dq_zero", s, [&] { return launch_bwd_dq_zero(b, s); });
     for (int t = 0; e == cudaSuccess && t < P; ++t)
         for (int kh = 0; e == cudaSuccess && kh < 2; ++kh) {
             b.ring_t = t;
             b.zz_kh = kh;
-            // dK, dV of KV chunk kh, one query half at a time (each CTA owns its key rows); every KV
-            // chunk is first written at t = 0 by query half 0
+            // KV chunk kh against one query half at a time (each CTA owns its key rows): dK, dV of the
+            // chunk (first written at t = 0 by query half 0) and the half's dQ partials
             for (int qh = 0; e == cudaSuccess && qh < 2; ++qh) {
                 b.zz_qh = qh;
                 b.n_outer = P * B;
                 b.accumulate = (t == 0 && qh == 0) ? 0 : 1;
-                e = traced("zigzag_bwd_dkdv", s, [&] { return launch_bwd_dkdv(b, s); });
+                e = traced("zigzag_bwd_dkdvq", s, [&] { return launch_bwd_dkdvq(b, s); });
             }
-            // dQ of both query halves against KV chunk kh; every query chunk is first written at t = 0, kh = 0
-            b.zz_qh = -1;
-            b.n_outer = 2 * P * B;
-            b.accumulate = (t == 0 && kh == 0) ? 0 : 1;
-            if (e == cudaSuccess) e = traced("zigzag_bwd_dq", s, [&] { return launch_bwd_dq(b, s); });
         }
-    if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dq, dq, (int64_t)q_elems, s); });
+    b.dq = dq;
+    if (e == cudaSuccess) e = traced("zigzag_bwd_dq_store", s, [&] { return launch_bwd_dq_store(b, s); });
     if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dk, dk, (int64_t)k_elems, s); });
     if (e == cudaSuccess) e = traced("ring_to_bf16", s, [&] { return launch_f32_to_bf16(acc_dv, dv, (int64_t)k_elems, s); });
     return cuda_status(e);
@@ -1169,8 +1173,9 @@ static size_t hybrid_bwd_rows(const usp_problem* p, int Pu) {
 
 size_t usp_hybrid_bwd_workspace_size(const usp_problem* p, int Pu) {
     if (hybrid_check(p, Pu) != USP_OK) return 0;
-    const size_t q_elems = (size_t)p->B * p->N * p->Hq * p->d, k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
-    return ring_part(hybrid_bwd_rows(p, Pu) * 40) + ring_part(q_elems * 4) + 2 * ring_part(k_elems * 4);
+    const size_t k_elems = (size_t)p->B * p->N * p->Hkv * p->d;
+    return ring_part(hybrid_bwd_rows(p, Pu) * 40) + ring_part(hybrid_bwd_rows(p, Pu) * p->d * 4) +
+           2 * ring_part(k_elems * 4);
 }
 
 usp_status usp_hybrid_attn_bwd(const usp_problem* p, int Pu, const void* q, const void* k, const void* v,
@@ -1183,10 +1188,10 @@ usp_status usp_hybrid_attn_bwd(const usp_problem* p, int Pu, const void* q, cons
     if (!sp) return USP_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int Pr = p->P / Pu, B = p->B, d = p->d, Nc = p->N / Pr, Hl = p->Hq / Pu;
-    const size_t q_elems = (size_t)B * p->N * p->Hq * d, k_elems = (size_t)B * p->N * p->Hkv * d;
+    const size_t k_elems = (size_t)B * p->N * p->Hkv * d;
     char* w = static_cast<char*>(ws);
     float* acc_dq = reinterpret_cast<float*>(w + ring_part(hybrid_bwd_rows(p, Pu) * 40));
-    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(q_elems * 4));
+    float* acc_dk = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dq) + ring_part(hybrid_bwd_rows(p, Pu) * d * 4));
     float* acc_dv = reinterpret_cast<float*>(reinterpret_cast<char*>(acc_dk) + ring_part(k_elems * 4));
 
     BwdParams b{};
@@ -1201,7 +1206,7 @@ usp_status usp_hybrid_attn_bwd(const usp_problem* p, int Pu, const void* q, cons
     b.l_s_outer = (int64_t)Hl * Nc;
     b.ws = reinterpret_cast<float*>(w);
     b.n_z = p->P * B * Hl;
-    b.dq_f32 = acc_dq;
+    b.dq_acc = acc_dq;
     b.dk_f32 = acc_dk;
     b.dv_f32 = acc_dv;
     b.d = d;
@@ -1213,9 +1218,7 @@ usp_status usp_hybrid_attn_bwd(const usp_problem* p, int Pu, const void* q, cons
 
     // as the ring backward, over groups: dK, dV travel with the KV chunk, dQ stays
     cudaError_t e = traced("hybrid_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    if (e == cudaSuccess)
-        e = ring_bwd_schedule(b, Pr, Pu * B, p->causal != 0, q_elems, k_elems, dq, dk, dv, "hybrid_bwd_dkdv",
-                              "hybrid_bwd_dq", s);
+    if (e == cudaSuccess) e = ring_bwd_schedule(b, Pr, Pu * B, p->causal != 0, k_elems, dq, dk, dv, "hybrid_bwd_dkdvq", s);
     return cuda_status(e);
 }
 

@@ -873,15 +873,27 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // columns after the element-wise warps have loaded dP^T(i), and dP^T(i+1) is
 // issued after they have drained dQ(i).  Per step the tensor core runs
 //     dK(i)  dQ(i)  | dV(i+1)  dP^T(i+1)  S^T(i+2) | dK(i+1) ...
-// and the element-wise warps compute P(i+1) while dK(i) and dQ(i) run,
-// drain dQ(i) while dV(i+1) runs, and dS(i+1) while S^T(i+2) runs.  Q tiles
+// and the element-wise warps compute P(i+1) while dK(i) and dQ(i) run and
+// dS(i+1) while S^T(i+2) runs; the reducer warps drain dQ(i) from TMEM while
+// dV(i+1) runs, then add it into the accumulator.  Q tiles
 // are released after dK, dO tiles (with dS^T) after dQ, so the next Q tile
 // loads while dQ and dV run.  The lse / D rows enter S^T and dP^T as the
 // ninth k-step of pass 2.
+// Sixteen warps in four warpgroups: 0 and 1 element-wise (P, dS), 2 the TMA producer (warp 8) and
+// the MMA issuer (warp 9), 3 the dQ reducers (warp w drains the TMEM lanes 32 (w % 4) .. + 31 of
+// dQ and adds them into the accumulator).  The reductions are throttled by the L2's atomic rate
+// (about 22 bytes per clock per SM against 64 KiB per step): on warps of their own they stall
+// only themselves, not the computation of P and dS.  Registers per thread after the set-up:
+// the launch gives 128 (65536 / 512), which the element-wise warps keep; warpgroup 2 gives 32
+// back, which the reducers take (each holds its 32 rows' d values of dQ).
 constexpr int kKqEwWarps = 8;
 constexpr int kKqProducerWarp = 8;
 constexpr int kKqMmaWarp = 9;
-constexpr int kKqThreads = 10 * 32;
+constexpr int kKqRedWarp0 = 12;
+constexpr int kKqThreads = 16 * 32;
+constexpr int kKqEwRegs = 65536 / kKqThreads, kKqOtherRegs = 96, kKqRedRegs = 160;
+static_assert(2 * kKqEwRegs + kKqOtherRegs + kKqRedRegs <= 4 * (65536 / kKqThreads),
+              "register split exceeds the launch allocation of a sub-partition");
 
 template <int D>
 struct KqCfg {
@@ -963,7 +975,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
         mbar_init(BAR(kDVDone), 1);
         mbar_init(BAR(kDSReady), kKqEwWarps * 32);
         mbar_init(BAR(kDQFull), 1);
-        mbar_init(BAR(kDQFree), kKqEwWarps * 32);
+        mbar_init(BAR(kDQFree), 4 * 32);  // the four reducer warps
         mbar_init(BAR(kOReady), 1);
         mbar_init(BAR(kDrain), 1);
         fence_mbar_init();
@@ -984,6 +996,10 @@ __global__ void __launch_bounds__(kKqThreads, 1)
     const uint32_t tmem = *tmem_slot;
     volatile int* abort_p = &abort_flag;
 
+    // Each role's code sits inside the branch that set its register budget; every warp of a
+    // warpgroup executes the same setmaxnreg.
+    if (warp >= kKqProducerWarp && warp < kKqRedWarp0) {
+        setmaxnreg_dec<kKqOtherRegs>();
     if (n_it > 0 && warp == kKqProducerWarp && lane == 0) {
         // ---------------------------------------------------------------- TMA producer
         tma_prefetch_desc(&tm_q);
@@ -1139,12 +1155,53 @@ __global__ void __launch_bounds__(kKqThreads, 1)
         // every issued MMA completes before TMEM is freed (after an abort, too)
         mma_commit(BAR(kDrain));
         mbar_drain(BAR(kDrain), 0, 62, p.status);
-    } else if (warp < kKqEwWarps) {
+    }
+    } else if (warp >= kKqRedWarp0) {
+        setmaxnreg_inc<kKqRedRegs>();
+        // ---------------------------------------------------------------- dQ reducers
+        // warp w: query rows 32 (w % 4) .. + 31 of the step's tile (TMEM lanes), every column
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + C::kColDP;
+        for (int it = 0; it < n_it; ++it) {
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kDQFull), it & 1, abort_p, 66, p.status))) break;
+            tc_fence_after();
+            uint32_t a[32], b[32];
+            tmem_ld32(lane_base, a);
+            tmem_ld32(lane_base + 32, b);
+            [[maybe_unused]] uint32_t c[32], e4[32];
+            if constexpr (D == 128) {
+                tmem_ld32(lane_base + 64, c);
+                tmem_ld32(lane_base + 96, e4);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(BAR(kDQFree));  // in registers: dP^T(it+1) may overwrite these columns
+            const int hq = hk * p.g + it / nq;
+            const int qt = qt_lo + it % nq;
+            // row r, column group g (columns 4 g .. 4 g + 3) at (g * 128 + r) * 4: for one g the
+            // warp's 32 rows are 512 contiguous bytes
+            float* row = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ + r) * 4;
+            auto red8 = [&](const uint32_t(&v)[32], int g0) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    red_add_v4(row + (int64_t)(g0 + g) * C::kBQ * 4, __uint_as_float(v[4 * g]),
+                               __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                               __uint_as_float(v[4 * g + 3]));
+            };
+            red8(a, 0);
+            red8(b, 8);
+            if constexpr (D == 128) {
+                red8(c, 16);
+                red8(e4, 24);
+            }
+        }
+    } else {
         // ---------------------------------------------------------------- element-wise warps
-        // warp w: TMEM lanes 32 (w % 4) .. + 31 (its key rows of S^T / dP^T, its query rows of dQ),
-        // query columns (and dQ columns) of half w / 4
+        // (the launch's register budget, kKqEwRegs)
+        // warp w: TMEM lanes 32 (w % 4) .. + 31 (its key rows of S^T / dP^T), query columns of half w / 4
         const int quad = warp & 3, half = warp >> 2;
-        const int krow = quad * 32 + lane;  // key row of S^T, dP^T and dS^T; query row of dQ
+        const int krow = quad * 32 + lane;  // key row of S^T, dP^T and dS^T
         const int key = kt * C::kBK + krow;
         const bool key_ok = key < p.Nkv;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
@@ -1218,32 +1275,10 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             mbar_arrive(BAR(kDSReady));
             return true;
         };
-        // dQ(j) from the dP^T columns (this warp's query rows, columns half * D/2 ..) into the accumulator
-        auto do_dq = [&](int j) -> bool {
-            if (!ew_wait(kDQFull, j & 1, 66)) return false;
-            tc_fence_after();
-            uint32_t ra[32], rb[32];
-            tmem_ld32(lane_base + C::kColDP + half * (D / 2), ra);
-            if constexpr (D == 128) tmem_ld32(lane_base + C::kColDP + half * (D / 2) + 32, rb);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(BAR(kDQFree));  // the values are in registers: dP^T(j+1) may overwrite them
-            const int hq = hk * p.g + j / nq;
-            const int qt = qt_lo + j % nq;
-            float* tile = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D;
-#pragma unroll
-            for (int e = 0; e < D / 8; ++e) {  // column group half * D/8 + e: columns 4 e .. of this half
-                const uint32_t* r = e < 8 ? &ra[4 * e] : &rb[4 * (e - 8)];
-                red_add_v4(tile + ((half * (D / 8) + e) * C::kBQ + krow) * 4, __uint_as_float(r[0]),
-                           __uint_as_float(r[1]), __uint_as_float(r[2]), __uint_as_float(r[3]));
-            }
-            return true;
-        };
         if (n_it > 0) ok = do_p(0) && do_ds(0);
-        for (int it = 0; ok && it < n_it; ++it) {
-            if (it + 1 < n_it && !do_p(it + 1)) { ok = false; break; }
-            if (!do_dq(it)) { ok = false; break; }
-            if (it + 1 < n_it && !do_ds(it + 1)) { ok = false; break; }
+        for (int it = 0; ok && it + 1 < n_it; ++it) {
+            if (!do_p(it + 1)) { ok = false; break; }
+            if (!do_ds(it + 1)) { ok = false; break; }
         }
         if (ok && n_it > 0) ok = ew_wait(kOReady, 0, 67);
         if (ok) {
@@ -1255,6 +1290,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
             const float mul = half == 0 ? 1.f : p.scale;
             uint16_t* out16 = half == 0 ? p.dv : p.dk;
+            float* out32 = half == 0 ? p.dv_f : p.dk_f;  // ring schedules: float32, added to when acc != 0
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t r[32];
@@ -1265,7 +1301,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = 0u;
                 }
-                if (valid) store_row32(out16, nullptr, 0, base + cc * 32, r, mul);
+                if (valid) store_row32(out16, out32, p.acc, base + cc * 32, r, mul);
             }
         }
     }
@@ -1439,7 +1475,7 @@ cudaError_t dq_t(const BwdParams& b, cudaStream_t stream) {
 
 template <int D, bool SPLIT>
 cudaError_t dkdvq_t(const BwdParams& b, cudaStream_t stream) {
-    if (!b.dq_acc || !b.dq) return cudaErrorInvalidValue;
+    if (!b.dq_acc) return cudaErrorInvalidValue;
     BwdMaps m;
     if (!make_bwd_maps<D>(b, KqCfg<D>::kBQ, &m)) return cudaErrorInvalidValue;
     auto kern = dkdvq_kernel<D, SPLIT>;
