@@ -1181,7 +1181,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             const int qt = qt_lo + it % nq;
             // row r, column group g (columns 4 g .. 4 g + 3) at (g * 128 + r) * 4: for one g the
             // warp's 32 rows are 512 contiguous bytes
-            float* row = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ + r) * 4;
+            float* row = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D + r * 4;
             auto red8 = [&](const uint32_t(&v)[32], int g0) {
 #pragma unroll
                 for (int g = 0; g < 8; ++g)
