@@ -865,17 +865,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 //   (the CTAs of the other key tiles add theirs; the order of the additions
 //   varies from run to run, so dQ is not bit-reproducible, unlike dK and dV,
 //   which stay in TMEM for the whole walk).
-// dS^T (bf16) goes to shared memory, where it is the A operand of both
-// dK += dS^T Q (K-major) and dQ = dS K (the same bytes read M-major).  At
-// d = 128 it is written over the dO tile of its own step once dV, the last
-// product reading that tile, is done (no room for a buffer of its own).
-// TMEM: S^T (P^T in place, bf16), dP^T, dV, dK; dQ(i) lands in the dP^T
-// columns after the element-wise warps have loaded dP^T(i), and dP^T(i+1) is
-// issued after they have drained dQ(i).  Per step the tensor core runs
-//     dK(i)  dQ(i)  | dV(i+1)  dP^T(i+1)  S^T(i+2) | dK(i+1) ...
+// dS^T (bf16) goes over the first half of each 64-column block of dP^T in
+// TMEM, the A operand of dK += dS^T Q, and to shared memory, where its bytes
+// read M-major are the A operand of dQ = dS K.  At d = 128 the shared copy is
+// written over the dO tile of its own step once dV, the last product reading
+// that tile, is done (no room for a buffer of its own).
+// TMEM: S^T (P^T in place, bf16), dP^T (dS^T in place), dV, dK; dQ(i) lands
+// in the dP^T columns after dK(i) has read dS^T(i) there, and dP^T(i+1) is
+// issued after the reducers have drained dQ(i).  Per step the tensor core runs
+//     dK(i)  dQ(i)  | dP^T(i+1)  dV(i+1)  S^T(i+2) | dK(i+1) ...
 // and the element-wise warps compute P(i+1) while dK(i) and dQ(i) run and
-// dS(i+1) while S^T(i+2) runs; the reducer warps drain dQ(i) from TMEM while
-// dV(i+1) runs, then add it into the accumulator.  Q tiles
+// dS(i+1) while dV(i+1) runs; the reducer warps drain dQ(i) from TMEM right
+// after dQ(i), then add it into the accumulator.  Q tiles
 // are released after dK, dO tiles (with dS^T) after dQ, so the next Q tile
 // loads while dQ and dV run.  The lse / D rows enter S^T and dP^T as the
 // ninth k-step of pass 2.
@@ -1081,14 +1082,14 @@ __global__ void __launch_bounds__(kKqThreads, 1)
                 mma_ts(tmem + C::kColDV, a, b0 + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
             }
         };
-        // dK += dS^T Q: A = dS^T K-major (queries 16 kk .. + 15), B = Q N-major
+        // dK += dS^T Q: A = dS^T from TMEM (the bf16 half of each 64-column block of dP^T), B = Q N-major
         auto issue_dk = [&](int it) {
-            const uint64_t a0 = sdesc_sw128(sbase + ds_off(it), 16, 1024);
             const uint64_t b0 = sdesc_sw128(sbase + C::kOffQ + (it % S) * C::kTile, 16384, 1024);
 #pragma unroll
-            for (int kk = 0; kk < C::kBQ / 16; ++kk)
-                mma_ss(tmem + C::kColDK, a0 + (((kk / 4) * 16384 + (kk % 4) * 32) >> 4), b0 + (kk * 2048 >> 4), kIdG,
-                       (it > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < C::kBQ / 16; ++kk) {
+                const uint32_t a = tmem + C::kColDP + (kk / 4) * 64 + (kk % 4) * 8;
+                mma_ts(tmem + C::kColDK, a, b0 + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
+            }
         };
         // dQ = dS K into the dP^T columns: A = the dS^T bytes read M-major (keys 16 kk .. + 15), B = K N-major
         auto issue_dq = [&](int it) {
@@ -1127,21 +1128,22 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             tc_fence_after();
             issue_dk(it);
             mma_commit(BAR(kQEmpty + s));
-            issue_dq(it);  // into the dP^T columns: the element-wise warps loaded dP^T(it) before dS(it)
+            issue_dq(it);  // over the dP^T columns: after dK(it), which read dS^T from them
             mma_commit(BAR(kDQFull));
             mma_commit(BAR(kOEmpty + s));
             if (it + 1 < n_it) {
                 const int s1 = (it + 1) % S;
-                if (!mbar_wait(BAR(kPReady), (it + 1) & 1, abort_p, 59, p.status)) break;
-                if (!mbar_wait(BAR(kOFull + s1), ((it + 1) / S) & 1, abort_p, 58, p.status)) break;
-                tc_fence_after();
-                issue_dv(it + 1);
-                mma_commit(BAR(kDVDone));
-                // dP^T(it+1) overwrites dQ(it): after the element-wise warps have drained it
+                // dP^T(it+1) overwrites dQ(it): after the reducers have drained it. It goes before
+                // dV(it+1), so that dS(it+1) is computed while dV(it+1) runs.
                 if (!mbar_wait(BAR(kDQFree), it & 1, abort_p, 61, p.status)) break;
+                if (!mbar_wait(BAR(kOFull + s1), ((it + 1) / S) & 1, abort_p, 58, p.status)) break;
                 tc_fence_after();
                 issue_t(it + 1, dv0, C::kOffDO, C::kColDP, 1);
                 mma_commit(BAR(kDPFull));
+                if (!mbar_wait(BAR(kPReady), (it + 1) & 1, abort_p, 59, p.status)) break;
+                tc_fence_after();
+                issue_dv(it + 1);
+                mma_commit(BAR(kDVDone));
                 if (it + 2 < n_it) {
                     if (!mbar_wait(BAR(kQFull + (it + 2) % S), ((it + 2) / S) & 1, abort_p, 57, p.status)) break;
                     tc_fence_after();
@@ -1262,7 +1264,10 @@ __global__ void __launch_bounds__(kKqThreads, 1)
                                                    __uint_as_float(e < 32 ? ra[e + 1] : rb[e - 31])));
                 pk[e / 2] = pack_bf16(ds.x, ds.y);
             }
-            // at d = 128 dS^T goes over this step's dO tile: wait until dV(j), its last reader, is done
+            // dS^T over the first 32 of this warp's dP^T columns: the A operand of dK (dP^T is in registers)
+            tmem_st32(lane_base + col_dp, pk);
+            // at d = 128 dS^T also goes over this step's dO tile (the A operand of dQ): wait until
+            // dV(j), its last reader, is done
             if (C::kDsInDo && !ew_wait(kDVDone, j & 1, 65)) return false;
             // row krow, queries 64 half .. + 63: one 128-byte row of the 128-byte-swizzled K-major tile
             uint8_t* row = smem + ds_off(j) + half * 16384 + krow * 128;
@@ -1271,6 +1276,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
                 *reinterpret_cast<uint4*>(row + ((u ^ (krow & 7)) << 4)) =
                     make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
             fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(kDSReady));
             return true;
