@@ -911,7 +911,11 @@ struct KqCfg {
     static constexpr int kOffQ = 2 * kTile;
     static constexpr int kOffDO = kOffQ + kStages * kTile;
     static constexpr int kOffDS = kOffDO + kStages * kTile;             // d = 64: dS^T's own buffer
-    static constexpr int kOffX = kOffDS + (kDsInDo ? 0 : kDsBytes);     // per stage: lse rows, D rows
+    // the reducers' staging of half of dQ (128 rows x 64 columns, float32): at d = 128 the dO tile of
+    // the step (dS^T's shared copy, free once dQ is done), at d = 64 a buffer of its own
+    static constexpr int kStageBytes = 128 * 64 * 4;
+    static constexpr int kOffStage = kOffDS + (kDsInDo ? 0 : kDsBytes);
+    static constexpr int kOffX = kOffStage + (kDsInDo ? 0 : kStageBytes);  // per stage: lse rows, D rows
     static constexpr int kOffOnes = kOffX + kStages * 2 * kXBytes;
     static constexpr int kOffZero = kOffOnes + kBK * 16;
     static constexpr int kOffBar = kOffZero + 2048;
@@ -921,10 +925,30 @@ struct KqCfg {
 };
 static_assert(KqCfg<128>::kSmemBytes <= 227 * 1024 && KqCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
 
-__device__ __forceinline__ void red_add_v4(float* a, float x, float y, float z, float w) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(a), "f"(x), "f"(y), "f"(z), "f"(w)
+// bytes of shared memory (16-byte aligned, a multiple of 16) added into global float32 memory by the
+// TMA engine, completion tracked by this thread's bulk-async group
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
                  : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// the four reducer warps (named barrier 1): every thread's flag ANDed
+__device__ __forceinline__ bool reducers_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void reducers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kKqThreads, 1)
@@ -1130,7 +1154,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             mma_commit(BAR(kQEmpty + s));
             issue_dq(it);  // over the dP^T columns: after dK(it), which read dS^T from them
             mma_commit(BAR(kDQFull));
-            mma_commit(BAR(kOEmpty + s));
+            if constexpr (!C::kDsInDo) mma_commit(BAR(kOEmpty + s));  // d = 128: the reducers release it
             if (it + 1 < n_it) {
                 const int s1 = (it + 1) % S;
                 // dP^T(it+1) overwrites dQ(it): after the reducers have drained it. It goes before
@@ -1161,43 +1185,50 @@ __global__ void __launch_bounds__(kKqThreads, 1)
     } else if (warp >= kKqRedWarp0) {
         setmaxnreg_inc<kKqRedRegs>();
         // ---------------------------------------------------------------- dQ reducers
-        // warp w: query rows 32 (w % 4) .. + 31 of the step's tile (TMEM lanes), every column
+        // warp w: query rows 32 (w % 4) .. + 31 of the step's tile (TMEM lanes), every column.  dQ(it)
+        // goes from TMEM to registers (then dP^T(it+1) may overwrite it), from registers to a shared
+        // staging buffer half a tile at a time ([16 column groups][128 rows][4]), and from there into
+        // the accumulator by the TMA engine's bulk reduction (its 32 KiB are contiguous there too).
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
+        const bool elected = warp == kKqRedWarp0 && lane == 0;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + C::kColDP;
         for (int it = 0; it < n_it; ++it) {
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kDQFull), it & 1, abort_p, 66, p.status))) break;
+            const bool ok_w = __all_sync(0xffffffffu, mbar_wait(BAR(kDQFull), it & 1, abort_p, 66, p.status));
+            if (!reducers_all(ok_w)) break;  // all four warps leave together (they share named barrier 1)
             tc_fence_after();
-            uint32_t a[32], b[32];
-            tmem_ld32(lane_base, a);
-            tmem_ld32(lane_base + 32, b);
-            [[maybe_unused]] uint32_t c[32], e4[32];
-            if constexpr (D == 128) {
-                tmem_ld32(lane_base + 64, c);
-                tmem_ld32(lane_base + 96, e4);
-            }
+            uint32_t v[D / 32][32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + c * 32, v[c]);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(BAR(kDQFree));  // in registers: dP^T(it+1) may overwrite these columns
             const int hq = hk * p.g + it / nq;
             const int qt = qt_lo + it % nq;
-            // row r, column group g (columns 4 g .. 4 g + 3) at (g * 128 + r) * 4: for one g the
-            // warp's 32 rows are 512 contiguous bytes
-            float* row = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D + r * 4;
-            auto red8 = [&](const uint32_t(&v)[32], int g0) {
+            float* tile = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D;
+            const uint32_t stage = sbase + (C::kDsInDo ? ds_off(it) : C::kOffStage);
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    red_add_v4(row + (int64_t)(g0 + g) * C::kBQ * 4, __uint_as_float(v[4 * g]),
-                               __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
-                               __uint_as_float(v[4 * g + 3]));
-            };
-            red8(a, 0);
-            red8(b, 8);
-            if constexpr (D == 128) {
-                red8(c, 16);
-                red8(e4, 24);
+            for (int h = 0; h < D / 64; ++h) {
+                // column groups 16 h .. 16 h + 15 of row r: the warp's 32 rows of one group are 512 bytes
+#pragma unroll
+                for (int g = 0; g < 16; ++g) {
+                    const uint32_t* x = &v[2 * h + g / 8][4 * (g % 8)];
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (g * C::kBQ + r) * 16),
+                                 "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                reducers_sync();
+                if (elected) {
+                    bulk_reduce_add_f32(tile + h * 16 * C::kBQ * 4, stage, C::kStageBytes);
+                    bulk_wait_read_all();  // the staging buffer may be written again
+                }
+                reducers_sync();
             }
+            // d = 128: the staging was this step's dO tile; the producer may load the next one into it
+            if (C::kDsInDo && elected) mbar_arrive(BAR(kOEmpty + it % S));
         }
+        if (elected) bulk_wait_all();  // every reduction issued has reached global memory
     } else {
         // ---------------------------------------------------------------- element-wise warps
         // (the launch's register budget, kKqEwRegs)
