@@ -911,8 +911,15 @@ struct KqCfg {
     static constexpr int kOffQ = 2 * kTile;
     static constexpr int kOffDO = kOffQ + kStages * kTile;
     static constexpr int kOffDS = kOffDO + kStages * kTile;             // d = 64: dS^T's own buffer
-    // the reducers' staging of half of dQ (128 rows x 64 columns, float32): at d = 128 the dO tile of
-    // the step (dS^T's shared copy, free once dQ is done), at d = 64 a buffer of its own
+    // dQ's column groups (4 columns of 128 rows each) reach the accumulator two ways: the last
+    // kRedGroups by red.global from the reducers' registers (through the SM's L1TEX unit, which the
+    // tensor core's operand reads also use), the others staged in shared memory and reduced by the
+    // TMA engine (which costs shared-memory bandwidth twice): splitting the traffic loads both paths
+    static constexpr int kGroups = D / 4;
+    static constexpr int kRedGroups = D == 128 ? 16 : 0;  // measured: 274 ms at d = 128 (0 or 32: 294, 311); none at d = 64
+    static constexpr bool kRedFirst = false;
+    // the staging buffer, up to 16 column groups (32 KiB) per round: at d = 128 the dO tile of the
+    // step (dS^T's shared copy, free once dQ is done), at d = 64 a buffer of its own
     static constexpr int kStageBytes = 128 * 64 * 4;
     static constexpr int kOffStage = kOffDS + (kDsInDo ? 0 : kDsBytes);
     static constexpr int kOffX = kOffStage + (kDsInDo ? 0 : kStageBytes);  // per stage: lse rows, D rows
@@ -1186,9 +1193,10 @@ __global__ void __launch_bounds__(kKqThreads, 1)
         setmaxnreg_inc<kKqRedRegs>();
         // ---------------------------------------------------------------- dQ reducers
         // warp w: query rows 32 (w % 4) .. + 31 of the step's tile (TMEM lanes), every column.  dQ(it)
-        // goes from TMEM to registers (then dP^T(it+1) may overwrite it), from registers to a shared
-        // staging buffer half a tile at a time ([16 column groups][128 rows][4]), and from there into
-        // the accumulator by the TMA engine's bulk reduction (its 32 KiB are contiguous there too).
+        // goes from TMEM to registers (then dP^T(it+1) may overwrite it); kRedGroups of its column
+        // groups go from there into the accumulator by red.global, the others through the shared
+        // staging buffer ([groups][128 rows][4]) and the TMA engine's bulk reduction (the same bytes
+        // are contiguous in the accumulator).
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const bool elected = warp == kKqRedWarp0 && lane == 0;
@@ -1207,12 +1215,26 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             const int qt = qt_lo + it % nq;
             float* tile = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D;
             const uint32_t stage = sbase + (C::kDsInDo ? ds_off(it) : C::kOffStage);
+            // column group g of row r sits at (g * 128 + r) * 4 floats of the tile
+            auto red_groups = [&]() {
+                float* rowp = tile + r * 4;
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                // column groups 16 h .. 16 h + 15 of row r: the warp's 32 rows of one group are 512 bytes
+                for (int g = C::kGroups - C::kRedGroups; g < C::kGroups; ++g) {
+                    const uint32_t* x = &v[g / 8][4 * (g % 8)];
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(rowp + g * C::kBQ * 4),
+                                 "f"(__uint_as_float(x[0])), "f"(__uint_as_float(x[1])), "f"(__uint_as_float(x[2])),
+                                 "f"(__uint_as_float(x[3]))
+                                 : "memory");
+                }
+            };
+            if (C::kRedFirst) red_groups();
 #pragma unroll
-                for (int g = 0; g < 16; ++g) {
-                    const uint32_t* x = &v[2 * h + g / 8][4 * (g % 8)];
+            for (int g0 = 0; g0 < C::kGroups - C::kRedGroups; g0 += 16) {
+                const int ng = C::kGroups - C::kRedGroups - g0 < 16 ? C::kGroups - C::kRedGroups - g0 : 16;
+                // groups g0 .. g0 + ng - 1 of row r: the warp's 32 rows of one group are 512 bytes
+#pragma unroll
+                for (int g = 0; g < ng; ++g) {
+                    const uint32_t* x = &v[(g0 + g) / 8][4 * ((g0 + g) % 8)];
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (g * C::kBQ + r) * 16),
                                  "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3])
                                  : "memory");
@@ -1220,11 +1242,12 @@ __global__ void __launch_bounds__(kKqThreads, 1)
                 fence_proxy_async_smem();
                 reducers_sync();
                 if (elected) {
-                    bulk_reduce_add_f32(tile + h * 16 * C::kBQ * 4, stage, C::kStageBytes);
+                    bulk_reduce_add_f32(tile + g0 * C::kBQ * 4, stage, (uint32_t)ng * C::kBQ * 16);
                     bulk_wait_read_all();  // the staging buffer may be written again
                 }
                 reducers_sync();
             }
+            if (!C::kRedFirst) red_groups();
             // d = 128: the staging was this step's dO tile; the producer may load the next one into it
             if (C::kDsInDo && elected) mbar_arrive(BAR(kOEmpty + it % S));
         }
