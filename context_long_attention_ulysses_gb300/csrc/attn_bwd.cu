@@ -1247,9 +1247,10 @@ __global__ void __launch_bounds__(kKqThreads, 1)
                 }
                 reducers_sync();
             }
-            if (!C::kRedFirst) red_groups();
             // d = 128: the staging was this step's dO tile; the producer may load the next one into it
+            // (before the red.global issue, which can wait on the L1TEX queue)
             if (C::kDsInDo && elected) mbar_arrive(BAR(kOEmpty + it % S));
+            if (!C::kRedFirst) red_groups();
         }
         if (elected) bulk_wait_all();  // every reduction issued has reached global memory
     } else {
