@@ -291,13 +291,12 @@ def kernel_work(name: str, w, launches: int):
         return "tensor", 1.5 * f               # S, dP, dQ: 6*d per visible pair
     if name == "attn_bwd_dkdvq":
         return "tensor", 2.5 * f               # S^T, dP^T, dV, dK, dQ: 10*d per visible pair
-    if name == "attn_bwd_dq_zero":
-        return "hbm", B * Hq * npad * d * 4    # the float32 dQ accumulator written
     if name == "attn_bwd_dq_store":
         return "hbm", B * Hq * npad * d * 4 + q_bytes  # the accumulator read, dQ (bf16) written
     if name == "attn_bwd_pre":
-        # reads O, dO and lse; writes D, lse*log2(e) (float32) and two 16-byte split rows per padded row
-        return "hbm", 2 * q_bytes + B * Hq * N * 4 + B * Hq * npad * (2 * 4 + 2 * 16)
+        # reads O, dO and lse; writes D, lse*log2(e) (float32) and two 16-byte split rows per padded
+        # row, and zeros the float32 dQ accumulator
+        return "hbm", 2 * q_bytes + B * Hq * N * 4 + B * Hq * npad * (2 * 4 + 2 * 16 + d * 4)
     if name in ("a2a_seq2head", "a2a_head2seq"):
         # per step: Q, K, V, dO in (one launch each), O, dQ, dK, dV out; read + write bytes
         per_step = {"a2a_seq2head": 2 * (2 * q_bytes + 2 * kv_bytes),

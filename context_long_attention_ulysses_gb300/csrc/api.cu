@@ -336,14 +336,13 @@ static BwdParams head_sharded_bwd(const usp_problem* p, const void* q, const voi
     return b;
 }
 
-// The one-pass backward: dQ accumulator zeroed, workspace rows, dK/dV/dQ-partials, dQ rounded.
-static cudaError_t one_pass_bwd(BwdParams b, const usp_problem* p, void* ws, const char* const names[4],
+// The one-pass backward: workspace rows with the dQ accumulator zeroed, dK/dV/dQ-partials, dQ rounded.
+static cudaError_t one_pass_bwd(BwdParams b, const usp_problem* p, void* ws, const char* const names[3],
                                 cudaStream_t s) {
     b.dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + bwd_rows_bytes(p));
-    cudaError_t e = traced(names[0], s, [&] { return launch_bwd_dq_zero(b, s); });
-    if (e == cudaSuccess) e = traced(names[1], s, [&] { return launch_bwd_pre(b, s); });
-    if (e == cudaSuccess) e = traced(names[2], s, [&] { return launch_bwd_dkdvq(b, s); });
-    if (e == cudaSuccess) e = traced(names[3], s, [&] { return launch_bwd_dq_store(b, s); });
+    cudaError_t e = traced(names[0], s, [&] { return launch_bwd_pre(b, s); });
+    if (e == cudaSuccess) e = traced(names[1], s, [&] { return launch_bwd_dkdvq(b, s); });
+    if (e == cudaSuccess) e = traced(names[2], s, [&] { return launch_bwd_dq_store(b, s); });
     return e;
 }
 
@@ -357,7 +356,7 @@ usp_status usp_attn_bwd(const usp_problem* p, const void* q, const void* k, cons
     int* sp = status_ptr();
     if (!sp) return USP_ERR_CUDA;
     const BwdParams b = head_sharded_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, sp);
-    static const char* const names[4] = {"attn_bwd_dq_zero", "attn_bwd_pre", "attn_bwd_dkdvq", "attn_bwd_dq_store"};
+    static const char* const names[3] = {"attn_bwd_pre", "attn_bwd_dkdvq", "attn_bwd_dq_store"};
     return cuda_status(one_pass_bwd(b, p, ws, names, static_cast<cudaStream_t>(stream)));
 }
 
@@ -426,11 +425,11 @@ static cudaError_t ring_fwd_schedule(FwdParams f, int n_groups, int per_member, 
 // masked only on the diagonal (t = 0).  Every block receives its first contribution at t = 0, so
 // later steps add.  The accumulators are rounded to bf16 once.
 // Every step runs the one-pass kernel: its dQ partials go into the float32 dQ accumulator b.dq_acc
-// (zeroed first, rounded to bf16 into dq at the end), its dK and dV into the float32 accumulators
+// (zeroed by the pre pass, rounded to bf16 into dq at the end), its dK and dV into the float32 accumulators
 // b.dk_f32 and b.dv_f32 (written at t = 0, added to after).
 static cudaError_t ring_bwd_schedule(BwdParams b, int n_groups, int per_member, bool causal, size_t k_elems,
                                      void* dq, void* dk, void* dv, const char* name_step, cudaStream_t s) {
-    cudaError_t e = traced("ring_bwd_dq_zero", s, [&] { return launch_bwd_dq_zero(b, s); });
+    cudaError_t e = cudaSuccess;
     for (int t = 0; e == cudaSuccess && t < n_groups; ++t) {
         b.ring_t = t;
         b.ring_i0 = causal ? t : 0;
@@ -717,7 +716,6 @@ usp_status usp_allgather_attn_bwd(const usp_problem* p, const void* q, const voi
     b.status = sp;
 
     cudaError_t e = traced("allgather_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    if (e == cudaSuccess) e = traced("allgather_bwd_dq_zero", s, [&] { return launch_bwd_dq_zero(b, s); });
     // dK, dV: rank i's partial over the gathered keys, summed over the ranks in float32 (the
     // reduce part of a reduce-scatter), one launch per rank in rank order; each launch also adds
     // rank i's dQ partials (dQ_i is complete after rank i's launch)
@@ -921,7 +919,6 @@ usp_status usp_zigzag_attn_bwd(const usp_problem* p, const void* q, const void* 
     b.status = sp;
 
     cudaError_t e = traced("zigzag_bwd_pre", s, [&] { return launch_bwd_pre(b, s); });
-    if (e == cudaSuccess) e = traced("zigzag_bwd_dq_zero", s, [&] { return launch_bwd_dq_zero(b, s); });
     for (int t = 0; e == cudaSuccess && t < P; ++t)
         for (int kh = 0; e == cudaSuccess && kh < 2; ++kh) {
             b.ring_t = t;
@@ -1042,8 +1039,7 @@ usp_status usp_fused_attn_bwd(const usp_problem* p, const void* q, const void* k
     b.split_b = B;
     b.scale = eff_scale(p);
     b.status = sp;
-    static const char* const names[4] = {"fused_bwd_dq_zero", "fused_bwd_pre", "fused_bwd_dkdvq",
-                                          "fused_bwd_dq_store"};
+    static const char* const names[3] = {"fused_bwd_pre", "fused_bwd_dkdvq", "fused_bwd_dq_store"};
     return cuda_status(one_pass_bwd(b, p, ws, names, static_cast<cudaStream_t>(stream)));
 }
 

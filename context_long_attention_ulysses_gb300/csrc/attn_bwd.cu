@@ -65,60 +65,80 @@ struct PreArgs {
     float scale;
     float *dvec, *lse2;
     uint4 *xl, *xd;
+    float* dq_acc;  // one-pass backward: the float32 dQ accumulator, zeroed here (null: left alone)
 };
 
-// One warp per padded row z * Npad + n (z = outer * heads + head): dvec = dO . O
-// (fp32), lse2 = lse * log2(e), and the split rows of lse / scale (xl) and of
-// dvec (xd).
+// One block per 128-row tile of padded rows z * Npad + n (z = outer * heads + head; Npad is a
+// multiple of 128, so a tile belongs to one z): dvec = dO . O (fp32), lse2 = lse * log2(e), the
+// split rows of lse / scale (xl) and of dvec (xd), and the tile's rows of the dQ accumulator set
+// to zero. Each row's O and dO are read as D/8 16-byte pieces by D/8 consecutive threads; every
+// thread issues all of its loads (two per row it covers) before it uses one, and the zero stores
+// while they are in flight.
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
-    if (row >= (int64_t)a.n_z * a.Npad) return;
-    const int z = (int)(row / a.Npad);
-    const int n = (int)(row % a.Npad);
+    constexpr int kPieces = D / 8;             // 16-byte pieces per row: 16 or 8
+    constexpr int kRowsPerPass = 256 / kPieces;  // 16 or 32
+    constexpr int kPasses = 128 / kRowsPerPass;  // 8 or 4
+    __shared__ float dot[128];
+    const int64_t row0 = (int64_t)blockIdx.x * 128;
+    const int z = (int)(row0 / a.Npad);
+    const int n0 = (int)(row0 % a.Npad);
     const int outer = z / a.heads, head = z % a.heads;
-    float* __restrict__ dvec = a.dvec;
-    float* __restrict__ lse2 = a.lse2;
-    uint4* __restrict__ xl = a.xl;
-    uint4* __restrict__ xd = a.xd;
+    const int piece = threadIdx.x % kPieces;
+    const int sub = threadIdx.x / kPieces;
     const int N = a.N;
-    if (n >= N) {
-        if (lane == 0) {
-            dvec[row] = 0.f;
-            lse2[row] = INFINITY;
-            xl[row] = make_uint4(0x0000FF7Fu, 0u, 0u, 0u);  // -(largest finite bf16): P underflows to 0
-            xd[row] = make_uint4(0u, 0u, 0u, 0u);
+    uint4 ov[kPasses], dv[kPasses];
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+        const int n = n0 + i * kRowsPerPass + sub;
+        ov[i] = make_uint4(0u, 0u, 0u, 0u);
+        dv[i] = ov[i];
+        if (n < N) {
+            const TokOuter at = split_pos(n, outer, SPLIT ? a.split_np : 0, a.split_b);
+            const int64_t base =
+                (int64_t)at.outer * a.s_outer + (int64_t)head * a.s_head + (int64_t)at.tok * a.s_tok + piece * 8;
+            ov[i] = __ldg(reinterpret_cast<const uint4*>(a.o + base));
+            dv[i] = __ldg(reinterpret_cast<const uint4*>(a.dout + base));
         }
-        return;
     }
-    constexpr int kPer = D / 32;  // elements per lane (2 or 4)
-    const TokOuter at = split_pos(n, outer, SPLIT ? a.split_np : 0, a.split_b);
-    const int64_t base = (int64_t)at.outer * a.s_outer + (int64_t)head * a.s_head + (int64_t)at.tok * a.s_tok + lane * kPer;
-    const uint16_t* __restrict__ o = a.o;
-    const uint16_t* __restrict__ dout = a.dout;
-    float acc = 0.f;
-    if constexpr (kPer == 4) {
-        const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-        const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
-        acc = __uint_as_float(a.x << 16) * __uint_as_float(b.x << 16) +
-              __uint_as_float(a.x & 0xFFFF0000u) * __uint_as_float(b.x & 0xFFFF0000u) +
-              __uint_as_float(a.y << 16) * __uint_as_float(b.y << 16) +
-              __uint_as_float(a.y & 0xFFFF0000u) * __uint_as_float(b.y & 0xFFFF0000u);
-    } else {
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base);
-        const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + base);
-        acc = __uint_as_float(a << 16) * __uint_as_float(b << 16) +
-              __uint_as_float(a & 0xFFFF0000u) * __uint_as_float(b & 0xFFFF0000u);
+    if (a.dq_acc) {
+        float4* t = reinterpret_cast<float4*>(a.dq_acc + row0 * D);
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int j = threadIdx.x; j < 128 * D / 4; j += 256) t[j] = zero;
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        const float l = a.lse[(int64_t)at.outer * a.l_s_outer + (int64_t)head * a.l_s_head + (int64_t)at.tok * a.l_s_tok];
-        dvec[row] = acc;
-        lse2[row] = l * kLog2e;
-        xl[row] = neg_split3(l / a.scale);
-        xd[row] = neg_split3(acc);
+    for (int i = 0; i < kPasses; ++i) {
+        const uint32_t* x = &ov[i].x;
+        const uint32_t* y = &dv[i].x;
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            acc += __uint_as_float(x[e] << 16) * __uint_as_float(y[e] << 16) +
+                   __uint_as_float(x[e] & 0xFFFF0000u) * __uint_as_float(y[e] & 0xFFFF0000u);
+#pragma unroll
+        for (int off = kPieces / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (piece == 0) dot[i * kRowsPerPass + sub] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        const int r = threadIdx.x;
+        const int n = n0 + r;
+        const int64_t row = row0 + r;
+        if (n >= N) {
+            a.dvec[row] = 0.f;
+            a.lse2[row] = INFINITY;
+            a.xl[row] = make_uint4(0x0000FF7Fu, 0u, 0u, 0u);  // -(largest finite bf16): P underflows to 0
+            a.xd[row] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            const TokOuter at = split_pos(n, outer, SPLIT ? a.split_np : 0, a.split_b);
+            const float l = a.lse[(int64_t)at.outer * a.l_s_outer + (int64_t)head * a.l_s_head + (int64_t)at.tok * a.l_s_tok];
+            const float acc = dot[r];
+            a.dvec[row] = acc;
+            a.lse2[row] = l * kLog2e;
+            a.xl[row] = neg_split3(l / a.scale);
+            a.xd[row] = neg_split3(acc);
+        }
     }
 }
 
@@ -1376,11 +1396,6 @@ __global__ void __launch_bounds__(kKqThreads, 1)
 }
 
 // The dQ accumulator to zero: 16-byte stores, grid-stride (n4 = float4 count).
-__global__ void __launch_bounds__(256) zero_f32x4_kernel(float4* dst, int64_t n4) {
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) dst[i] = z;
-}
-
 // dQ = scale * accumulator, rounded to bf16: thread (tile, part, row) converts columns 32 part .. + 31
 // of one query row (reads of consecutive threads are consecutive 16-byte groups of the tile).
 template <int D, bool SPLIT>
@@ -1500,9 +1515,10 @@ cudaError_t pre_t(const BwdParams& b, cudaStream_t stream) {
     a.lse2 = const_cast<float*>(p.lse2);
     a.xl = const_cast<uint4*>(p.xl);
     a.xd = const_cast<uint4*>(p.xd);
-    const int64_t rows = (int64_t)b.n_z * p.Npad;
-    if (rows == 0) return cudaSuccess;
-    bwd_pre_kernel<D, SPLIT><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
+    a.dq_acc = b.dq_acc;
+    const int64_t tiles = (int64_t)b.n_z * p.Npad / 128;
+    if (tiles == 0) return cudaSuccess;
+    bwd_pre_kernel<D, SPLIT><<<(unsigned)tiles, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -1593,14 +1609,6 @@ struct DqStoreF {
 cudaError_t launch_bwd_pre(const BwdParams& b, cudaStream_t stream) { return dispatch<PreF>(b, stream); }
 cudaError_t launch_bwd_dkdv(const BwdParams& b, cudaStream_t stream) { return dispatch<DkdvF>(b, stream); }
 cudaError_t launch_bwd_dq(const BwdParams& b, cudaStream_t stream) { return dispatch<DqF>(b, stream); }
-cudaError_t launch_bwd_dq_zero(const BwdParams& b, cudaStream_t stream) {
-    if (!b.dq_acc) return cudaErrorInvalidValue;
-    const int64_t n4 = (int64_t)b.n_z * npad_of(b) * b.d / 4;  // 128-row tiles of d values: a multiple of 4
-    if (n4 == 0) return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, 152 * 8);
-    zero_f32x4_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<float4*>(b.dq_acc), n4);
-    return cudaGetLastError();
-}
 cudaError_t launch_bwd_dkdvq(const BwdParams& b, cudaStream_t stream) { return dispatch<DkdvqF>(b, stream); }
 cudaError_t launch_bwd_dq_store(const BwdParams& b, cudaStream_t stream) { return dispatch<DqStoreF>(b, stream); }
 

@@ -113,11 +113,10 @@ struct BwdParams {
 cudaError_t launch_bwd_pre(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdParams& p, cudaStream_t stream);
-// The one-pass backward (bf16 results only), in this order: the dQ accumulator zeroed
-// (launch_bwd_dq_zero) and the workspace rows (launch_bwd_pre), dK, dV and the dQ partials of
-// every block pair (launch_bwd_dkdvq), then dQ = scale * accumulator rounded to bf16
+// The one-pass backward (bf16 results only), in this order: the workspace rows with the dQ
+// accumulator zeroed (launch_bwd_pre, when p.dq_acc is set), dK, dV and the dQ partials of every
+// block pair (launch_bwd_dkdvq), then dQ = scale * accumulator rounded to bf16
 // (launch_bwd_dq_store).
-cudaError_t launch_bwd_dq_zero(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dkdvq(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_store(const BwdParams& p, cudaStream_t stream);
 
