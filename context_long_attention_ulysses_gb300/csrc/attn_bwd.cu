@@ -939,16 +939,23 @@ struct KqCfg {
     static constexpr int kRedGroups = D == 128 ? 16 : 0;  // measured: 274 ms at d = 128 (0 or 32: 294, 311); none at d = 64
     static constexpr bool kRedFirst = false;
     // the staging buffer, up to 16 column groups (32 KiB) per round: at d = 128 the dO tile of the
-    // step (dS^T's shared copy, free once dQ is done), at d = 64 a buffer of its own
+    // step (dS^T's shared copy, free once dQ is done), at d = 64 two buffers of their own used in
+    // turn (a step's bulk reduction may still be reading one while the next step fills the other)
     static constexpr int kStageBytes = 128 * 64 * 4;
     static constexpr int kOffStage = kOffDS + (kDsInDo ? 0 : kDsBytes);
-    static constexpr int kOffX = kOffStage + (kDsInDo ? 0 : kStageBytes);  // per stage: lse rows, D rows
+    static constexpr int kOffX = kOffStage + (kDsInDo ? 0 : 2 * kStageBytes);  // per stage: lse rows, D rows
+    static_assert(kDsInDo || kGroups - kRedGroups <= 16, "d = 64: one staging round per step");
     static constexpr int kOffOnes = kOffX + kStages * 2 * kXBytes;
     static constexpr int kOffZero = kOffOnes + kBK * 16;
     static constexpr int kOffBar = kOffZero + 2048;
     static constexpr int kNumBars = 1 + 4 * kStages + 9;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+    // dQ's columns: at d = 128 the dP^T columns (TMEM is full), so that dP^T(it+1) waits until the
+    // reducers have drained dQ(it); at d = 64 columns of its own (448 .. 511), so that only dQ(it+1)
+    // waits for that (measured at 128K: 206.3 ms against 212.2)
+    static constexpr bool kDqOwn = D == 64;
+    static constexpr uint32_t kColDQ = kDqOwn ? 448 : kColDP;
 };
 static_assert(KqCfg<128>::kSmemBytes <= 227 * 1024 && KqCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -1142,12 +1149,12 @@ __global__ void __launch_bounds__(kKqThreads, 1)
                 mma_ts(tmem + C::kColDK, a, b0 + (kk * 2048 >> 4), kIdG, (it > 0 || kk > 0) ? 1u : 0u);
             }
         };
-        // dQ = dS K into the dP^T columns: A = the dS^T bytes read M-major (keys 16 kk .. + 15), B = K N-major
+        // dQ = dS K into its columns: A = the dS^T bytes read M-major (keys 16 kk .. + 15), B = K N-major
         auto issue_dq = [&](int it) {
             const uint64_t a0 = sdesc_sw128(sbase + ds_off(it), 16384, 1024);
 #pragma unroll
             for (int kk = 0; kk < C::kBK / 16; ++kk)
-                mma_ss(tmem + C::kColDP, a0 + (kk * 2048 >> 4), k_mn + (kk * 2048 >> 4), kIdQ, kk > 0 ? 1u : 0u);
+                mma_ss(tmem + C::kColDQ, a0 + (kk * 2048 >> 4), k_mn + (kk * 2048 >> 4), kIdQ, kk > 0 ? 1u : 0u);
         };
         bool ok = mbar_wait(BAR(kKvFull), 0, abort_p, 56, p.status);
         ok = ok && mbar_wait(BAR(kQFull), 0, abort_p, 57, p.status);
@@ -1179,14 +1186,17 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             tc_fence_after();
             issue_dk(it);
             mma_commit(BAR(kQEmpty + s));
-            issue_dq(it);  // over the dP^T columns: after dK(it), which read dS^T from them
+            // d = 64: dQ(it-1) drained from dQ's own columns; d = 128: over the dP^T columns, after
+            // dK(it), which read dS^T from them
+            if (C::kDqOwn && it > 0 && !mbar_wait(BAR(kDQFree), (it - 1) & 1, abort_p, 61, p.status)) break;
+            issue_dq(it);
             mma_commit(BAR(kDQFull));
             if constexpr (!C::kDsInDo) mma_commit(BAR(kOEmpty + s));  // d = 128: the reducers release it
             if (it + 1 < n_it) {
                 const int s1 = (it + 1) % S;
-                // dP^T(it+1) overwrites dQ(it): after the reducers have drained it. It goes before
-                // dV(it+1), so that dS(it+1) is computed while dV(it+1) runs.
-                if (!mbar_wait(BAR(kDQFree), it & 1, abort_p, 61, p.status)) break;
+                // d = 128: dP^T(it+1) overwrites dQ(it), after the reducers have drained it. It goes
+                // before dV(it+1), so that dS(it+1) is computed while dV(it+1) runs.
+                if (!C::kDqOwn && !mbar_wait(BAR(kDQFree), it & 1, abort_p, 61, p.status)) break;
                 if (!mbar_wait(BAR(kOFull + s1), ((it + 1) / S) & 1, abort_p, 58, p.status)) break;
                 tc_fence_after();
                 issue_t(it + 1, dv0, C::kOffDO, C::kColDP, 1);
@@ -1213,14 +1223,15 @@ __global__ void __launch_bounds__(kKqThreads, 1)
         setmaxnreg_inc<kKqRedRegs>();
         // ---------------------------------------------------------------- dQ reducers
         // warp w: query rows 32 (w % 4) .. + 31 of the step's tile (TMEM lanes), every column.  dQ(it)
-        // goes from TMEM to registers (then dP^T(it+1) may overwrite it); kRedGroups of its column
+        // goes from TMEM to registers (then dQ(it+1), or at d = 128 dP^T(it+1), may overwrite it);
+        // kRedGroups of its column
         // groups go from there into the accumulator by red.global, the others through the shared
         // staging buffer ([groups][128 rows][4]) and the TMA engine's bulk reduction (the same bytes
         // are contiguous in the accumulator).
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const bool elected = warp == kKqRedWarp0 && lane == 0;
-        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + C::kColDP;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + C::kColDQ;
         for (int it = 0; it < n_it; ++it) {
             const bool ok_w = __all_sync(0xffffffffu, mbar_wait(BAR(kDQFull), it & 1, abort_p, 66, p.status));
             if (!reducers_all(ok_w)) break;  // all four warps leave together (they share named barrier 1)
@@ -1230,11 +1241,16 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + c * 32, v[c]);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(BAR(kDQFree));  // in registers: dP^T(it+1) may overwrite these columns
+            mbar_arrive(BAR(kDQFree));  // in registers: the MMA may overwrite these columns
             const int hq = hk * p.g + it / nq;
             const int qt = qt_lo + it % nq;
             float* tile = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D;
-            const uint32_t stage = sbase + (C::kDsInDo ? ds_off(it) : C::kOffStage);
+            const uint32_t stage = sbase + (C::kDsInDo ? ds_off(it) : C::kOffStage + (it & 1) * C::kStageBytes);
+            if (!C::kDsInDo) {
+                // the buffer of step it - 2: its bulk reduction has read it (one group may still be in flight)
+                if (elected) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                reducers_sync();
+            }
             // column group g of row r sits at (g * 128 + r) * 4 floats of the tile
             auto red_groups = [&]() {
                 float* rowp = tile + r * 4;
@@ -1263,9 +1279,9 @@ __global__ void __launch_bounds__(kKqThreads, 1)
                 reducers_sync();
                 if (elected) {
                     bulk_reduce_add_f32(tile + g0 * C::kBQ * 4, stage, (uint32_t)ng * C::kBQ * 16);
-                    bulk_wait_read_all();  // the staging buffer may be written again
+                    if (C::kDsInDo) bulk_wait_read_all();  // the staging buffer may be written again
                 }
-                reducers_sync();
+                if (C::kDsInDo) reducers_sync();
             }
             // d = 128: the staging was this step's dO tile; the producer may load the next one into it
             // (before the red.global issue, which can wait on the L1TEX queue)
