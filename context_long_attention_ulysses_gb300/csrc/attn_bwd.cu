@@ -904,17 +904,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // the MMA issuer (warp 9), 3 the dQ reducers (warp w drains the TMEM lanes 32 (w % 4) .. + 31 of
 // dQ and adds them into the accumulator).  The reductions are throttled by the L2's atomic rate
 // (about 22 bytes per clock per SM against 64 KiB per step): on warps of their own they stall
-// only themselves, not the computation of P and dS.  Registers per thread after the set-up:
-// the launch gives 128 (65536 / 512), which the element-wise warps keep; warpgroup 2 gives 32
-// back, which the reducers take (each holds its 32 rows' d values of dQ).
+// only themselves, not the computation of P and dS.  Registers per thread after the set-up (the
+// launch gives 128, 65536 / 512): warpgroup 2 keeps KqCfg::kOtherRegs, the reducers take
+// kRedRegs (each holds its 32 rows' d values of dQ) and the two element-wise warpgroups kEwRegs.
 constexpr int kKqEwWarps = 8;
 constexpr int kKqProducerWarp = 8;
 constexpr int kKqMmaWarp = 9;
 constexpr int kKqRedWarp0 = 12;
 constexpr int kKqThreads = 16 * 32;
-constexpr int kKqEwRegs = 65536 / kKqThreads, kKqOtherRegs = 96, kKqRedRegs = 160;
-static_assert(2 * kKqEwRegs + kKqOtherRegs + kKqRedRegs <= 4 * (65536 / kKqThreads),
-              "register split exceeds the launch allocation of a sub-partition");
+constexpr int kKqLaunchRegs = 65536 / kKqThreads;
 
 template <int D>
 struct KqCfg {
@@ -951,6 +949,11 @@ struct KqCfg {
     static constexpr int kNumBars = 1 + 4 * kStages + 9;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+    // register budgets (setmaxnreg): warpgroup 2 gives 32 back, which the reducers take; the
+    // element-wise warps keep the launch's 128 (measured at d = 64: 144 for the reducers and 136 for
+    // the element-wise warps, 206.5 ms against 206.2)
+    static constexpr int kOtherRegs = 96, kRedRegs = 160;
+    static constexpr int kEwRegs = (4 * kKqLaunchRegs - kOtherRegs - kRedRegs) / 2 / 8 * 8;
     // dQ's columns: at d = 128 the dP^T columns (TMEM is full), so that dP^T(it+1) waits until the
     // reducers have drained dQ(it); at d = 64 columns of its own (448 .. 511), so that only dQ(it+1)
     // waits for that (measured at 128K: 206.3 ms against 212.2)
@@ -958,6 +961,9 @@ struct KqCfg {
     static constexpr uint32_t kColDQ = kDqOwn ? 448 : kColDP;
 };
 static_assert(KqCfg<128>::kSmemBytes <= 227 * 1024 && KqCfg<64>::kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(2 * KqCfg<128>::kEwRegs + KqCfg<128>::kOtherRegs + KqCfg<128>::kRedRegs <= 4 * kKqLaunchRegs &&
+                  2 * KqCfg<64>::kEwRegs + KqCfg<64>::kOtherRegs + KqCfg<64>::kRedRegs <= 4 * kKqLaunchRegs,
+              "register split exceeds the launch allocation of a sub-partition");
 
 // bytes of shared memory (16-byte aligned, a multiple of 16) added into global float32 memory by the
 // TMA engine, completion tracked by this thread's bulk-async group
@@ -1058,7 +1064,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
     // Each role's code sits inside the branch that set its register budget; every warp of a
     // warpgroup executes the same setmaxnreg.
     if (warp >= kKqProducerWarp && warp < kKqRedWarp0) {
-        setmaxnreg_dec<kKqOtherRegs>();
+        setmaxnreg_dec<C::kOtherRegs>();
     if (n_it > 0 && warp == kKqProducerWarp && lane == 0) {
         // ---------------------------------------------------------------- TMA producer
         tma_prefetch_desc(&tm_q);
@@ -1220,7 +1226,7 @@ __global__ void __launch_bounds__(kKqThreads, 1)
         mbar_drain(BAR(kDrain), 0, 62, p.status);
     }
     } else if (warp >= kKqRedWarp0) {
-        setmaxnreg_inc<kKqRedRegs>();
+        if constexpr (C::kRedRegs > kKqLaunchRegs) setmaxnreg_inc<C::kRedRegs>();
         // ---------------------------------------------------------------- dQ reducers
         // warp w: query rows 32 (w % 4) .. + 31 of the step's tile (TMEM lanes), every column.  dQ(it)
         // goes from TMEM to registers (then dQ(it+1), or at d = 128 dP^T(it+1), may overwrite it);
@@ -1290,8 +1296,8 @@ __global__ void __launch_bounds__(kKqThreads, 1)
         }
         if (elected) bulk_wait_all();  // every reduction issued has reached global memory
     } else {
+        if constexpr (C::kEwRegs > kKqLaunchRegs) setmaxnreg_inc<C::kEwRegs>();
         // ---------------------------------------------------------------- element-wise warps
-        // (the launch's register budget, kKqEwRegs)
         // warp w: TMEM lanes 32 (w % 4) .. + 31 (its key rows of S^T / dP^T), query columns of half w / 4
         const int quad = warp & 3, half = warp >> 2;
         const int krow = quad * 32 + lane;  // key row of S^T, dP^T and dS^T
