@@ -71,9 +71,8 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # default instantiations' (in-place sequence-sharded addressing compiled out); an
 # edit confined to the other instantiation (if constexpr) re-keys them unchanged.
 MEASURED_TRAFFIC = {
-    "attn_fwd": (2924220160 + 1160072448, "060417e63914f8b5", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdv": (9132134144 + 526144000, "2fc572cbac4bdfc6", ("attn_bwd.cu", "ptx.cuh")),
-    "attn_bwd_dq": (4461772800 + 1050943488, "2fc572cbac4bdfc6", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_fwd": (2917253000 + 1161101000, "6c5ca19b311ce5c0", ("attn_fwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdvq": (17574630000 + 8758665000, "5fac412a0a869bc4", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 

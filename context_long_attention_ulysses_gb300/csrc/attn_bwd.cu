@@ -937,11 +937,14 @@ struct KqCfg {
     static constexpr int kRedGroups = D == 128 ? 16 : 0;  // measured: 274 ms at d = 128 (0 or 32: 294, 311); none at d = 64
     static constexpr bool kRedFirst = false;
     // the staging buffer, up to 16 column groups (32 KiB) per round: at d = 128 the dO tile of the
-    // step (dS^T's shared copy, free once dQ is done), at d = 64 two buffers of their own used in
-    // turn (a step's bulk reduction may still be reading one while the next step fills the other)
+    // step (dS^T's shared copy, free once dQ is done), at d = 64 kStageBufs buffers of their own used
+    // in turn, each waited for (its bulk reduction's read) only when the reducers next fill it.
+    // Measured at 128K, d = 64: one buffer 204.3 ms, two 206.4 ms, one with a third Q/dO stage
+    // 206.5 ms.
     static constexpr int kStageBytes = 128 * 64 * 4;
+    static constexpr int kStageBufs = kDsInDo ? 0 : 1;
     static constexpr int kOffStage = kOffDS + (kDsInDo ? 0 : kDsBytes);
-    static constexpr int kOffX = kOffStage + (kDsInDo ? 0 : 2 * kStageBytes);  // per stage: lse rows, D rows
+    static constexpr int kOffX = kOffStage + kStageBufs * kStageBytes;  // per stage: lse rows, D rows
     static_assert(kDsInDo || kGroups - kRedGroups <= 16, "d = 64: one staging round per step");
     static constexpr int kOffOnes = kOffX + kStages * 2 * kXBytes;
     static constexpr int kOffZero = kOffOnes + kBK * 16;
@@ -1251,10 +1254,16 @@ __global__ void __launch_bounds__(kKqThreads, 1)
             const int hq = hk * p.g + it / nq;
             const int qt = qt_lo + it % nq;
             float* tile = p.dq_acc + (((int64_t)q_outer * p.Hq + hq) * p.Npad + (int64_t)qt * C::kBQ) * D;
-            const uint32_t stage = sbase + (C::kDsInDo ? ds_off(it) : C::kOffStage + (it & 1) * C::kStageBytes);
+            const uint32_t stage =
+                sbase + (C::kDsInDo ? ds_off(it)
+                                    : C::kOffStage + (it % (C::kStageBufs > 1 ? C::kStageBufs : 1)) * C::kStageBytes);
             if (!C::kDsInDo) {
-                // the buffer of step it - 2: its bulk reduction has read it (one group may still be in flight)
-                if (elected) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                // the buffer's previous step (it - kStageBufs): its bulk reduction has read it (with two
+                // buffers, the other step's group may still be in flight)
+                if (elected) {
+                    if constexpr (C::kStageBufs == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    else asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                }
                 reducers_sync();
             }
             // column group g of row r sits at (g * 128 + r) * 4 floats of the tile
