@@ -357,19 +357,25 @@ def run_usp(args, world, rank, local):
     ws = torch.empty(usp.usp_attn_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
     host_out = [torch.empty(t.shape, dtype=bf, pin_memory=True) for t in (o_seq, dq_seq, dk_seq, dv_seq)]
 
-    def step_on(ins, outs):
-        qs, ks, vs, dos = ins
-        os_, dqs, dks, dvs = outs
+    def fwd_on(ins, outs):
+        qs, ks, vs, _ = ins
         usp.usp_a2a_seq2head(p, Hq, qs, qh, sh)
         usp.usp_a2a_seq2head(p, Hkv, ks, kh, sh)
         usp.usp_a2a_seq2head(p, Hkv, vs, vh, sh)
         usp.usp_attn_fwd(p, qh, kh, vh, oh, lse, sh)
-        usp.usp_a2a_head2seq(p, Hq, oh, os_, sh)
-        usp.usp_a2a_seq2head(p, Hq, dos, doh, sh)
+        usp.usp_a2a_head2seq(p, Hq, oh, outs[0], sh)
+
+    def bwd_on(ins, outs):
+        _, dqs, dks, dvs = outs
+        usp.usp_a2a_seq2head(p, Hq, ins[3], doh, sh)
         usp.usp_attn_bwd(p, qh, kh, vh, oh, lse, doh, dqh, dkh, dvh, ws, None, sh)
         usp.usp_a2a_head2seq(p, Hq, dqh, dqs, sh)
         usp.usp_a2a_head2seq(p, Hkv, dkh, dks, sh)
         usp.usp_a2a_head2seq(p, Hkv, dvh, dvs, sh)
+
+    def step_on(ins, outs):
+        fwd_on(ins, outs)
+        bwd_on(ins, outs)
 
     ins0, outs0 = (q_seq, k_seq, v_seq, do_seq), (o_seq, dq_seq, dk_seq, dv_seq)
 
@@ -377,36 +383,53 @@ def run_usp(args, world, rank, local):
         step_on(ins0, outs0)
 
     # end to end, pipelined over steps: step i's inputs go host -> device on one copy stream while
-    # step i-1 computes, and step i's results go device -> host on another as soon as it is done.
-    # Two buffer sets on the device; every step's bytes still cross the host link in the timed region.
+    # step i-1 computes (Q, K, V first: the forward starts when they have landed, while dO is still
+    # on its way), and step i's results go device -> host on another as soon as each is ready (O
+    # while the backward runs, then dQ, dK, dV). Two buffer sets on the device; every step's bytes
+    # still cross the host link in the timed region.
     in_sets = [ins0, tuple(torch.empty_like(t) for t in ins0)]
     out_sets = [outs0, tuple(torch.empty_like(t) for t in outs0)]
     h2d_stream, d2h_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
     def e2e_steps(n, start_event):
-        h2d_done = [torch.cuda.Event() for _ in range(n)]
+        qkv_done = [torch.cuda.Event() for _ in range(n)]
+        do_done = [torch.cuda.Event() for _ in range(n)]
+        fwd_done = [torch.cuda.Event() for _ in range(n)]
         comp_done = [torch.cuda.Event() for _ in range(n)]
+        o_back = [torch.cuda.Event() for _ in range(n)]
         d2h_done = [torch.cuda.Event() for _ in range(n)]
 
         def h2d(i):
             h2d_stream.wait_event(start_event if i < 2 else comp_done[i - 2])  # set i % 2 released by step i-2
             with torch.cuda.stream(h2d_stream):
-                for dst, src in zip(in_sets[i % 2], host_in):
+                for dst, src in zip(in_sets[i % 2][:3], host_in[:3]):
                     dst.copy_(src, non_blocking=True)
-            h2d_done[i].record(h2d_stream)
+                qkv_done[i].record(h2d_stream)
+                in_sets[i % 2][3].copy_(host_in[3], non_blocking=True)
+                do_done[i].record(h2d_stream)
 
         h2d(0)
         for i in range(n):
             if i + 1 < n:
                 h2d(i + 1)
-            stream.wait_event(h2d_done[i])
+            ins, outs = in_sets[i % 2], out_sets[i % 2]
+            stream.wait_event(qkv_done[i])
             if i >= 2:
-                stream.wait_event(d2h_done[i - 2])  # output set i % 2 read back
-            step_on(in_sets[i % 2], out_sets[i % 2])
+                stream.wait_event(o_back[i - 2])  # O of set i % 2 read back
+            fwd_on(ins, outs)
+            fwd_done[i].record(stream)
+            d2h_stream.wait_event(fwd_done[i])
+            with torch.cuda.stream(d2h_stream):
+                host_out[0].copy_(outs[0], non_blocking=True)
+                o_back[i].record(d2h_stream)
+            stream.wait_event(do_done[i])
+            if i >= 2:
+                stream.wait_event(d2h_done[i - 2])  # gradients of set i % 2 read back
+            bwd_on(ins, outs)
             comp_done[i].record(stream)
             d2h_stream.wait_event(comp_done[i])
             with torch.cuda.stream(d2h_stream):
-                for dst, src in zip(host_out, out_sets[i % 2]):
+                for dst, src in zip(host_out[1:], outs[1:]):
                     dst.copy_(src, non_blocking=True)
             d2h_done[i].record(d2h_stream)
         stream.wait_event(d2h_done[n - 1])  # the last results are on the host
@@ -454,10 +477,15 @@ def run_usp(args, world, rank, local):
     e2e_steps(2, w0)  # warm the copy streams
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    e2e_steps(args.steps, e0)
-    e1.record(stream)
-    barrier()
+    usp.usp_trace_reset()
+    usp.usp_trace_enable(True)
+    with ClockSampler(gpu_uuid_or_index(torch, local)) as e2e_clk:
+        e0.record(stream)
+        e2e_steps(args.steps, e0)
+        e1.record(stream)
+        barrier()
+    usp.usp_trace_enable(False)
+    e2e_trace = usp.usp_trace_report()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
@@ -533,7 +561,10 @@ def run_usp(args, world, rank, local):
         "kernels": kernels,
         "gpu_launches": launches,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                # the compute stream's kernels inside the end-to-end region, and the clocks there
+                "kernels_ms_per_step": sum(v_[1] for v_ in e2e_trace.values()) / args.steps,
+                "clocks": e2e_clk.summary()},
         "clocks": clocks,
     }
     if ring is not None:
