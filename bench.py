@@ -597,7 +597,10 @@ def run_usp(args, world, rank, local):
 def bench_config_leg(usp, torch, dev, peaks, w, dtype, backward, steps=20, warmup=3):
     """One of the smaller workloads through the same Ulysses path as the step: remaps of Q, K, V,
     attention forward, remap of O, and with backward the remap of dO, the backward and the remaps of
-    dQ, dK, dV.  Inputs are seeded and resident; CUDA events around `steps` steps after `warmup`."""
+    dQ, dK, dV.  Inputs are seeded and resident; CUDA events around `steps` steps after `warmup`,
+    launched one by one; then the per-kernel times from a second, traced pass; then the same step
+    captured once into a CUDA graph and replayed `steps` times (these workloads are launch-bound:
+    a few microseconds of work per kernel)."""
     import numpy as np
     import synth
     p = usp.Problem(**w, causal=True, dtype=dtype)
@@ -619,33 +622,48 @@ def bench_config_leg(usp, torch, dev, peaks, w, dtype, backward, steps=20, warmu
     s = torch.cuda.current_stream()
     sh = s.cuda_stream
 
-    def step():
-        usp.usp_a2a_seq2head(p, Hq, qs, qh, sh)
-        usp.usp_a2a_seq2head(p, Hkv, ks, kh, sh)
-        usp.usp_a2a_seq2head(p, Hkv, vs, vh, sh)
-        usp.usp_attn_fwd(p, qh, kh, vh, oh, lse, sh)
-        usp.usp_a2a_head2seq(p, Hq, oh, os_, sh)
+    def step(sh_=sh):
+        usp.usp_a2a_seq2head(p, Hq, qs, qh, sh_)
+        usp.usp_a2a_seq2head(p, Hkv, ks, kh, sh_)
+        usp.usp_a2a_seq2head(p, Hkv, vs, vh, sh_)
+        usp.usp_attn_fwd(p, qh, kh, vh, oh, lse, sh_)
+        usp.usp_a2a_head2seq(p, Hq, oh, os_, sh_)
         if backward:
-            usp.usp_a2a_seq2head(p, Hq, dos, doh, sh)
-            usp.usp_attn_bwd(p, qh, kh, vh, oh, lse, doh, dqh, dkh, dvh, ws, None, sh)
-            usp.usp_a2a_head2seq(p, Hq, dqh, dqs, sh)
-            usp.usp_a2a_head2seq(p, Hkv, dkh, dks, sh)
-            usp.usp_a2a_head2seq(p, Hkv, dvh, dvs, sh)
+            usp.usp_a2a_seq2head(p, Hq, dos, doh, sh_)
+            usp.usp_attn_bwd(p, qh, kh, vh, oh, lse, doh, dqh, dkh, dvh, ws, None, sh_)
+            usp.usp_a2a_head2seq(p, Hq, dqh, dqs, sh_)
+            usp.usp_a2a_head2seq(p, Hkv, dkh, dks, sh_)
+            usp.usp_a2a_head2seq(p, Hkv, dvh, dvs, sh_)
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(steps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
 
     for _ in range(warmup):
         step()
-    torch.cuda.synchronize()
+    ms = timed(step)
     usp.usp_trace_reset()
     usp.usp_trace_enable(True)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(steps):
-        step()
-    e1.record(s)
-    torch.cuda.synchronize()
+    timed(step)
     usp.usp_trace_enable(False)
     trace = usp.usp_trace_report()
-    ms = e0.elapsed_time(e1) / steps
+    graph_ms, graph_err = None, None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(torch.cuda.current_stream().cuda_stream)
+        g.replay()
+        graph_ms = timed(g.replay)
+        del g
+    except Exception as e:  # the eager numbers stand; say why there is no graph figure
+        graph_err = f"{type(e).__name__}: {e}"[:200]
+        torch.cuda.synchronize()
     ok = usp.usp_device_status(sh) == 0
     f = (3.5 if backward else 1.0) * fwd_flops(w)
     esz = 2 if dtype == "bf16" else 4
@@ -662,6 +680,11 @@ def bench_config_leg(usp, torch, dev, peaks, w, dtype, backward, steps=20, warmu
                      "frac_of_8TBps": remap_gbs / 8000.0 if remap_gbs else None},
            "kernels_ms_per_step": {k_: v_[1] / steps for k_, v_ in trace.items()},
            "launches_per_step": sum(v_[0] for v_ in trace.values()) // steps,
+           "timing": "launches one by one, untraced; kernels_ms_per_step from a second, traced pass",
+           "graph": ({"ms_per_step": graph_ms, "TFLOPs": f / (graph_ms * 1e-3) / 1e12,
+                      "tokens_per_s": w["B"] * w["N"] / (graph_ms * 1e-3),
+                      "timing": "the step captured once into a CUDA graph, replayed steps times"}
+                     if graph_ms else {"unavailable": graph_err}),
            "steps": steps, "warmup": warmup, "status_ok": ok}
     if dtype == "bf16":
         leg["frac_sustained"] = tflops / peaks["bf16_sus"]

@@ -491,6 +491,62 @@ def test_hybrid_reduces_to_ulysses_and_ring_bitwise(usp):
 
 
 # ---------------------------------------------------------------- failure detection
+def test_step_captured_in_a_cuda_graph(usp):
+    """The whole Ulysses step (remaps, forward, backward, remaps back) captured once into a CUDA
+    graph and replayed gives the eagerly launched step's results: O, dK, dV bit for bit, dQ to one
+    bf16 unit (its float32 partial sums are added in an order that varies). Every call only
+    enqueues work on the stream it is given, so a caller can capture it."""
+    import torch
+    B, Hq, Hkv, N, d, P = 1, 8, 2, 1280, 128, 2
+    p = usp.Problem(B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, P=P)
+    q, k, v, dO = gen((B, Hq, N, d), 40), gen((B, Hkv, N, d), 41), gen((B, Hkv, N, d), 42), gen((B, Hq, N, d), 43)
+    qs, ks, vs, dos = (to_dev(to_seq(x, P)) for x in (q, k, v, dO))
+    bf = torch.bfloat16
+    qh, oh, doh, dqh = (torch.empty(p.head_shape(Hq), dtype=bf, device="cuda") for _ in range(4))
+    kh, vh, dkh, dvh = (torch.empty(p.head_shape(Hkv), dtype=bf, device="cuda") for _ in range(4))
+    lse = torch.empty(p.lse_head_shape(), dtype=torch.float32, device="cuda")
+    outs = [torch.empty_like(qs), torch.empty_like(qs), torch.empty_like(ks), torch.empty_like(vs)]
+    ws = torch.empty(usp.usp_attn_bwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+
+    def step(sh):
+        usp.usp_a2a_seq2head(p, Hq, qs, qh, sh)
+        usp.usp_a2a_seq2head(p, Hkv, ks, kh, sh)
+        usp.usp_a2a_seq2head(p, Hkv, vs, vh, sh)
+        usp.usp_attn_fwd(p, qh, kh, vh, oh, lse, sh)
+        usp.usp_a2a_head2seq(p, Hq, oh, outs[0], sh)
+        usp.usp_a2a_seq2head(p, Hq, dos, doh, sh)
+        usp.usp_attn_bwd(p, qh, kh, vh, oh, lse, doh, dqh, dkh, dvh, ws, None, sh)
+        usp.usp_a2a_head2seq(p, Hq, dqh, outs[1], sh)
+        usp.usp_a2a_head2seq(p, Hkv, dkh, outs[2], sh)
+        usp.usp_a2a_head2seq(p, Hkv, dvh, outs[3], sh)
+
+    step(torch.cuda.current_stream().cuda_stream)
+    _sync()
+    eager = [t.clone() for t in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(torch.cuda.current_stream().cuda_stream)
+    for t in outs:
+        t.zero_()
+    g.replay()
+    _sync()
+    _status_ok(usp)
+    for i in (0, 2, 3):
+        assert torch.equal(outs[i].view(torch.int16), eager[i].view(torch.int16))
+    assert bf16_ulp_diff(to_host(outs[1]), to_host(eager[1])) <= 1.0
+    # a replay after new inputs are written into the captured buffers follows them
+    qs.copy_(to_dev(to_seq(gen((B, Hq, N, d), 44), P)))
+    g.replay()
+    _sync()
+    replayed = [t.clone() for t in outs]
+    step(torch.cuda.current_stream().cuda_stream)
+    _sync()
+    _status_ok(usp)
+    assert not torch.equal(replayed[0], eager[0])
+    for i in (0, 2, 3):
+        assert torch.equal(replayed[i].view(torch.int16), outs[i].view(torch.int16))
+
+
 def test_bounded_wait_times_out_and_the_context_survives(usp):
     """A wait that nothing completes gives up after the 2 s limit: the host reads USP_ERR_TIMEOUT,
     the word is cleared, and the next work on the same context runs and is correct."""
