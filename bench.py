@@ -72,7 +72,7 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 # edit confined to the other instantiation (if constexpr) re-keys them unchanged.
 MEASURED_TRAFFIC = {
     "attn_fwd": (2917253000 + 1161101000, "6c5ca19b311ce5c0", ("attn_fwd.cu", "ptx.cuh")),
-    "attn_bwd_dkdvq": (17574630000 + 8758665000, "5fac412a0a869bc4", ("attn_bwd.cu", "ptx.cuh")),
+    "attn_bwd_dkdvq": (17574630000 + 8758665000, "b9836edb865ad03e", ("attn_bwd.cu", "ptx.cuh")),
 }
 
 

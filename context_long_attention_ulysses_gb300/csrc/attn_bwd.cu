@@ -68,12 +68,32 @@ struct PreArgs {
     float* dq_acc;  // one-pass backward: the float32 dQ accumulator, zeroed here (null: left alone)
 };
 
-// One block per 128-row tile of padded rows z * Npad + n (z = outer * heads + head; Npad is a
-// multiple of 128, so a tile belongs to one z): dvec = dO . O (fp32), lse2 = lse * log2(e), the
-// split rows of lse / scale (xl) and of dvec (xd), and the tile's rows of the dQ accumulator set
-// to zero. Each row's O and dO are read as D/8 16-byte pieces by D/8 consecutive threads; every
-// thread issues all of its loads (two per row it covers) before it uses one, and the zero stores
-// while they are in flight.
+// One block per 128 padded rows z * Npad + n (z = outer * heads + head; Npad is a multiple of
+// 128): dvec = dO . O (fp32), lse2 = lse * log2(e), the split rows of lse / scale (xl) and of dvec
+// (xd), and one 128-row tile of the dQ accumulator (tile = block) set to zero. Each row's O and dO
+// are read as D/8 16-byte pieces by D/8 consecutive threads; every thread issues all of its loads
+// (two per row it covers) before it uses one, and the zero stores while they are in flight.
+//
+// Which (outer, head, position) the block's row L (0 .. n_z * Npad - 1) covers: in the head-sharded
+// layout head-major (L = z * Npad + n, one block = 128 positions of one head), in the sequence-
+// sharded layout (SPLIT) token-major (L = (outer * Npad + n) * heads + head), so that a block's rows
+// are the heads of a few tokens, contiguous there.
+template <bool SPLIT>
+__device__ __forceinline__ void pre_row(const PreArgs& a, int64_t L, int& outer, int& head, int& n) {
+    if constexpr (SPLIT) {
+        const int64_t per_outer = (int64_t)a.Npad * a.heads;
+        outer = (int)(L / per_outer);
+        const int64_t rem = L - (int64_t)outer * per_outer;
+        n = (int)(rem / a.heads);
+        head = (int)(rem - (int64_t)n * a.heads);
+    } else {
+        const int z = (int)(L / a.Npad);
+        n = (int)(L - (int64_t)z * a.Npad);
+        outer = z / a.heads;
+        head = z - outer * a.heads;
+    }
+}
+
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
     constexpr int kPieces = D / 8;             // 16-byte pieces per row: 16 or 8
@@ -81,16 +101,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
     constexpr int kPasses = 128 / kRowsPerPass;  // 8 or 4
     __shared__ float dot[128];
     const int64_t row0 = (int64_t)blockIdx.x * 128;
-    const int z = (int)(row0 / a.Npad);
-    const int n0 = (int)(row0 % a.Npad);
-    const int outer = z / a.heads, head = z % a.heads;
     const int piece = threadIdx.x % kPieces;
     const int sub = threadIdx.x / kPieces;
     const int N = a.N;
     uint4 ov[kPasses], dv[kPasses];
 #pragma unroll
     for (int i = 0; i < kPasses; ++i) {
-        const int n = n0 + i * kRowsPerPass + sub;
+        int outer, head, n;
+        pre_row<SPLIT>(a, row0 + i * kRowsPerPass + sub, outer, head, n);
         ov[i] = make_uint4(0u, 0u, 0u, 0u);
         dv[i] = ov[i];
         if (n < N) {
@@ -123,8 +141,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
     __syncthreads();
     if (threadIdx.x < 128) {
         const int r = threadIdx.x;
-        const int n = n0 + r;
-        const int64_t row = row0 + r;
+        int outer, head, n;
+        pre_row<SPLIT>(a, row0 + r, outer, head, n);
+        const int64_t row = ((int64_t)outer * a.heads + head) * a.Npad + n;  // the workspace row
         if (n >= N) {
             a.dvec[row] = 0.f;
             a.lse2[row] = INFINITY;
