@@ -785,7 +785,7 @@ def bench_allgather(usp, torch, dev, peaks, w):
 
 def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
     """Two variants of the step on its workload: the all-to-all fused into the attention kernels
-    (no remap launches; two timed passes, each after a pass of the remapped step), and 2-D
+    (no remap launches; timed in alternation with the remapped step, four passes each), and 2-D
     sequence parallelism (Ulysses inside groups of Pu = P/2 ranks, ring across the 2 groups; one
     untimed and one timed pass)."""
     import numpy as np
@@ -847,7 +847,10 @@ def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
     fused_pass()
     remapped_pass()
     fwd_ms, bwd_ms, remapped_ms = [], [], []
-    n_pairs = 3
+    # ABBA order (remapped, fused, fused, remapped, ...): a clock that drifts over the leg weighs on
+    # both arms alike
+    order = "RFFRRFFR"
+    n_pairs = len(order) // 2
     ftrace, rtrace = {}, {}
 
     def add_trace(acc):
@@ -856,19 +859,17 @@ def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
             a_[0] += v_[0]
             a_[1] += v_[1]
 
-    for _ in range(n_pairs):
+    for arm in order:
         usp.usp_trace_reset()
         usp.usp_trace_enable(True)
-        remapped_ms.append(remapped_pass())
+        if arm == "R":
+            remapped_ms.append(remapped_pass())
+        else:
+            a, b = fused_pass()
+            fwd_ms.append(a)
+            bwd_ms.append(b)
         usp.usp_trace_enable(False)
-        add_trace(rtrace)
-        usp.usp_trace_reset()
-        usp.usp_trace_enable(True)
-        a, b = fused_pass()
-        usp.usp_trace_enable(False)
-        add_trace(ftrace)
-        fwd_ms.append(a)
-        bwd_ms.append(b)
+        add_trace(rtrace if arm == "R" else ftrace)
     ffwd, fbwd, rms = sum(fwd_ms) / n_pairs, sum(bwd_ms) / n_pairs, sum(remapped_ms) / n_pairs
     ok = usp.usp_device_status(sh) == 0
     del lse, ws, qh, kh, vh, oh, doh, dqh, dkh, dvh, lse_h
@@ -884,8 +885,8 @@ def bench_fused_and_hybrid(usp, torch, dev, peaks, w):
              "remapped_kernels_ms_per_step": {k_: v_[1] / n_pairs for k_, v_ in rtrace.items()},
              "remapped_kernels_sum_ms_per_step": sum(v_[1] for v_ in rtrace.values()) / n_pairs,
              "launches_per_step": sum(v_[0] for v_ in ftrace.values()) // n_pairs, "status_ok": ok,
-             "timing": f"mean of {n_pairs} passes, each after one pass of the remapped step on the same "
-                       "inputs; per-kernel times from the library's event tracer in both"}
+             "timing": f"mean of {n_pairs} passes of each, in the order {order} (R remapped, F fused) on the "
+                       "same inputs; per-kernel times from the library's event tracer in both"}
 
     # ---- 2-D: all-to-all inside 2 groups of P/2 ranks, ring over the 2 groups, all-to-all back
     Pu = max(1, P // 2)
