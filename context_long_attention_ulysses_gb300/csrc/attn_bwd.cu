@@ -10,7 +10,12 @@
 //   dK_j  = scale sum_{h in group} sum_i dS_ij Q_i
 //   dQ_i  = scale sum_j dS_ij K_j
 //
-// Three launches, no atomics, deterministic:
+// Two forms. usp_attn_bwd runs the one-pass form: pre (below, which also zeroes
+// a float32 dQ accumulator), then one kernel per (KV head, 128-key tile) that
+// computes S^T and dP^T once per block pair and produces dK, dV and the pair's
+// dQ partial (dkdvq_kernel, whose comment gives its design), then dQ rounded to
+// bf16.  usp_attn_bwd_deterministic runs the three-pass form, no atomics,
+// bit-reproducible:
 //  1. pre:  D_i and lse_i*log2(e) into a workspace padded to 128-row tiles
 //           (padding rows: lse = +inf, so their P is exactly 0), and -lse_i/scale
 //           and -D_i each as a sum of three bf16 numbers: one extra k-step of
@@ -909,9 +914,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // read M-major are the A operand of dQ = dS K.  At d = 128 the shared copy is
 // written over the dO tile of its own step once dV, the last product reading
 // that tile, is done (no room for a buffer of its own).
-// TMEM: S^T (P^T in place, bf16), dP^T (dS^T in place), dV, dK; dQ(i) lands
-// in the dP^T columns after dK(i) has read dS^T(i) there, and dP^T(i+1) is
-// issued after the reducers have drained dQ(i).  Per step the tensor core runs
+// TMEM: S^T (P^T in place, bf16), dP^T (dS^T in place), dV, dK; at d = 128 dQ(i)
+// lands in the dP^T columns after dK(i) has read dS^T(i) there, and dP^T(i+1) is
+// issued after the reducers have drained dQ(i) (at d = 64 dQ has columns of its
+// own, and only dQ(i+1) waits for that).  Per step the tensor core runs
 //     dK(i)  dQ(i)  | dP^T(i+1)  dV(i+1)  S^T(i+2) | dK(i+1) ...
 // and the element-wise warps compute P(i+1) while dK(i) and dQ(i) run and
 // dS(i+1) while dV(i+1) runs; the reducer warps drain dQ(i) from TMEM right
